@@ -1,0 +1,101 @@
+/*
+ * fa.h -- C ABI of the fused exact attention forward for GB300 (sm_103a).
+ *
+ * The operation ("FlashAttention 优化原理与实现要点解析" §1, §2, §4.3, §5, §7):
+ *
+ *     S = scale * Q K^T            (per batch b and head h; never written to memory)
+ *     S[i, j] = -inf  for j > i    (only when causal: a query sees keys at positions <= its own)
+ *     P = softmax(S) row-wise
+ *     O = P V
+ *     LSE[i] = m_i + ln(l_i),  m_i = max_j S[i, j],  l_i = sum_j exp(S[i, j] - m_i)
+ *
+ * computed tile by tile with online softmax: the running row maximum m and sum l are
+ * rescaled by exp(m_old - m_new) as each K/V tile arrives, the unnormalised O is rescaled by
+ * the same factor, and O is divided by l once at the end (same page §4.2, §4.3, §6). The
+ * statistics m and l are the ones the forward keeps for the backward pass
+ * ("FlashAttention V2 核心原理与架构设计" §2.3); they are returned combined as one fp32
+ * log-sum-exp per row, in natural-log units of the scaled scores.
+ *
+ * Layout. q, k, v, o: [B, N, H, d], dense and contiguous: element (b, n, h, c) sits at
+ * ((b*N + n)*H + h)*d + c. This is the [B, N, H, D] layout of the page's PyTorch wrapper
+ * ("FlashAttention V2 核心原理与架构设计" §5.2). lse: [B, H, N] fp32, element (b, h, n) at
+ * (b*H + h)*N + n.
+ *
+ * Ownership. Every pointer is a device pointer owned by the caller. The library allocates
+ * no device memory per call and frees nothing. Calls are asynchronous: fa_fwd only enqueues
+ * work on `stream` and returns.
+ *
+ * Threading. The entry points are thread-safe; per-device state (the device-side error word,
+ * the kernel attributes) is set up on first use of each device.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. NULL means the legacy default stream. */
+typedef struct CUstream_st* fa_stream_t;
+
+/* Storage type of q, k, v and o (lse is always fp32). */
+enum fa_dtype {
+    FA_BF16 = 0,
+    FA_FP16 = 1
+};
+
+/* Return codes. 0 is success; every error is negative. */
+enum fa_status {
+    FA_OK = 0,
+    FA_ERR_NULL = -1,     /* a required pointer is NULL */
+    FA_ERR_SHAPE = -2,    /* B, H or N < 1; d not 64 or 128; or B*N*H*d does not fit int64 */
+    FA_ERR_DTYPE = -3,    /* dtype is not an fa_dtype */
+    FA_ERR_ALIGN = -4,    /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
+    FA_ERR_ALIAS = -5,    /* o or lse overlaps q, k or v, or o overlaps lse */
+    FA_ERR_ARCH = -6,     /* the current device is not compute capability 10.3 (sm_103) */
+    FA_ERR_LAUNCH = -7,   /* the kernel launch failed (the CUDA error is not cleared) */
+    FA_ERR_TIMEOUT = -8,  /* a kernel wait ran past its limit; outputs are undefined */
+    FA_ERR_SCALE = -9,    /* scale is not finite */
+    FA_ERR_CUDA = -10     /* a CUDA runtime or driver query failed */
+};
+
+/*
+ * fa_fwd -- O = softmax(scale * Q K^T [+ causal mask]) V and LSE, for all B*H heads.
+ *
+ *   q, k, v  [B, N, H, d] dtype, device, 16-byte aligned, read only
+ *   o        [B, N, H, d] dtype, device, 16-byte aligned, written (every element)
+ *   lse      [B, H, N] fp32, device, 4-byte aligned, written (every element)
+ *   B, H, N  batch, heads, sequence length (>= 1 each); queries and keys share N
+ *   d        head dimension: 64 or 128
+ *   causal   0: every query sees all N keys; nonzero: query i sees keys 0..i
+ *   scale    multiplier of Q K^T, used as given (typically 1/sqrt(d)); must be finite
+ *   dtype    FA_BF16 or FA_FP16; the matrix products take this type, accumulate in fp32,
+ *            and the probabilities P are rounded to this type before P V
+ *   stream   CUDA stream the work is enqueued on
+ *
+ * Returns FA_OK once the work is enqueued. On a host-detected error (every code except
+ * FA_ERR_TIMEOUT) nothing is enqueued and the outputs are untouched. Kernel waits are bounded:
+ * if one runs out, the kernel records FA_ERR_TIMEOUT in a per-device error word (read it with
+ * fa_get_device_error) and exits without hanging the device.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+           int N, int d, int causal, float scale, int dtype, fa_stream_t stream);
+
+/* Static English text for a status code (never NULL). */
+const char* fa_error_string(int code);
+
+/*
+ * fa_get_device_error -- synchronise `stream`, then return and clear the current device's
+ * error word: FA_OK when no kernel wait has run out since the last call, FA_ERR_TIMEOUT
+ * otherwise, FA_ERR_CUDA when the synchronisation or the read failed.
+ */
+int fa_get_device_error(fa_stream_t stream);
+
+/* ABI version of this header: 1. */
+int fa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

@@ -1,0 +1,160 @@
+"""ctypes binding over the C ABI in ``include/fa.h`` (argument marshalling only).
+
+Every step of the attention forward runs in the CUDA library. This module turns torch tensors
+into device pointers and sizes, calls the library, and turns nonzero status codes into
+``FaError``. PyTorch only provides device memory and streams here.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libfa_gb300.so"
+
+FA_BF16, FA_FP16 = 0, 1
+FA_OK = 0
+FA_ERR_TIMEOUT = -8
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    """A nonzero status from the CUDA library."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (where, error_string(code), code))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "_build", LIB_NAME)
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the built CUDA library; raise if it has not been built. There is no fallback."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise FileNotFoundError(
+                    "CUDA library %s is missing: build it with "
+                    "io_aware_attention_fa2_gb300.build.build()" % path)
+            lib = ctypes.CDLL(path)
+            vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
+            lib.fa_fwd.restype = i32
+            lib.fa_error_string.argtypes = [i32]
+            lib.fa_error_string.restype = ctypes.c_char_p
+            lib.fa_get_device_error.argtypes = [vp]
+            lib.fa_get_device_error.restype = i32
+            lib.fa_abi_version.argtypes = []
+            lib.fa_abi_version.restype = i32
+            _lib = lib
+    return _lib
+
+
+def available() -> bool:
+    """True when the library is built and a CUDA device is visible."""
+    try:
+        import torch
+        load_library()
+        return torch.cuda.is_available()
+    except (OSError, ImportError):
+        return False
+
+
+def error_string(code: int) -> str:
+    try:
+        return load_library().fa_error_string(int(code)).decode()
+    except OSError:
+        return "status %d" % code
+
+
+def _stream_handle(stream) -> int | None:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float16:
+        return FA_FP16
+    raise TypeError("q, k, v must be bfloat16 or float16, got %s" % t.dtype)
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """Enqueue the attention forward on ``stream`` (default: torch's current stream).
+
+    q, k, v, o: CUDA tensors [B, N, H, d] of one dtype (bf16/fp16), contiguous.
+    lse: CUDA float32 tensor [B, H, N], contiguous.
+    """
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, N, H, d]")
+    B, N, H, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o)):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("%s must match q's shape and dtype" % name)
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32:
+        raise ValueError("lse must be float32 [B, H, N]")
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    rc = load_library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                               _dtype_code(q), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+
+
+def device_error(stream=None) -> int:
+    """Synchronise ``stream`` and return-and-clear the device error word (0 = none)."""
+    return int(load_library().fa_get_device_error(_stream_handle(stream)))
+
+
+def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
+                      lse=None, stream=None, device=None):
+    """O, LSE = attention(q, k, v). The call a user makes.
+
+    Device tensors are used in place. Host tensors (ideally pinned) are copied to ``device``
+    (default cuda:0) on ``stream``, the kernel runs there, and O and LSE are copied back into
+    host tensors, so the result is ready when the call returns. ``scale`` defaults to
+    1/sqrt(d) rounded to fp32.
+    """
+    import math
+
+    import torch
+    B, N, H, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+    if q.is_cuda:
+        o = out if out is not None else torch.empty_like(q)
+        ls = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32,
+                                                     device=q.device)
+        fa_fwd(q, k, v, o, ls, causal, scale, stream)
+        return o, ls
+    dev = torch.device(device or "cuda:0")
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.stream(st):
+        qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
+        od = torch.empty_like(qd)
+        ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        fa_fwd(qd, kd, vd, od, ld, causal, scale, st)
+        o_host = out if out is not None else torch.empty(q.shape, dtype=q.dtype,
+                                                         pin_memory=q.is_pinned())
+        l_host = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32,
+                                                         pin_memory=q.is_pinned())
+        o_host.copy_(od, non_blocking=True)
+        l_host.copy_(ld, non_blocking=True)
+    st.synchronize()
+    return o_host, l_host

@@ -1,0 +1,189 @@
+/*
+ * attn_oracle.c -- plain fp64 CPU attention: the oracle for the fused attention forward.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the benchmark's CPU-baseline
+ * leg load this file's library. The product path (the CUDA library) never calls it, and the
+ * two share no code, header, table or constant.
+ *
+ * What it computes is the plain definition of scaled dot-product attention, evaluated in
+ * double precision on the exact values of the bf16/fp16 inputs:
+ *
+ *   "FlashAttention 优化原理与实现要点解析" §1: Attention(Q,K,V) = Softmax(Q K^T / sqrt(d)) V,
+ *       here with the caller's scale in place of 1/sqrt(d).
+ *   same page §2: three steps, S = Q K^T, P = Softmax(S), O = P V, materialising S and P
+ *       (one row of each at a time: row i of O depends only on row i of S and P).
+ *   same page §4.1: Softmax(x_i) = e^{x_i} / sum_j e^{x_j}, evaluated as the three passes it
+ *       lists: (1) the row maximum m, (2) the sum l = sum_j e^{x_j - m}, (3) e^{x_i - m} / l.
+ *   same page §7: causal masking, a query attends only to keys at positions <= its own.
+ *   "FlashAttention V2 核心原理与架构设计" §2.3: the kernel also keeps the per-row softmax
+ *       denominator l and row maximum m; the oracle reports them as one log-sum-exp,
+ *       LSE_i = m_i + ln(l_i), in units of scaled scores.
+ *
+ * Layouts: q, k, v and o are [B, N, H, d] row-major (element (b, n, h, c) at
+ * ((b*N + n)*H + h)*d + c); lse is [B, H, N]. Keys at positions >= N do not exist. With
+ * `causal`, key j is allowed for query i only when j <= i.
+ *
+ * There is no blocking, fusion or reordering here: one (b, h, i) row at a time, the three
+ * passes in order. Rows are independent, so OpenMP spreads rows over host cores.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_F64 = 0, ORACLE_BF16 = 1, ORACLE_FP16 = 2 };
+
+/* bfloat16 is the upper half of an IEEE binary32: sign, 8 exponent bits, 7 mantissa bits. */
+static double bf16_bits_value(uint16_t bits) {
+    uint32_t w = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* IEEE binary16: sign, 5 exponent bits (bias 15), 10 mantissa bits. */
+static double fp16_bits_value(uint16_t bits) {
+    int sign = (bits >> 15) & 1;
+    int expo = (bits >> 10) & 0x1f;
+    int mant = bits & 0x3ff;
+    double mag;
+    if (expo == 0)
+        mag = ldexp((double)mant, -24);                 /* subnormal: mant * 2^-14 * 2^-10 */
+    else if (expo == 31)
+        mag = mant ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(1024 + mant), expo - 25);  /* (1 + mant/1024) * 2^(expo-15) */
+    return sign ? -mag : mag;
+}
+
+static double elem(const void* base, int kind, int64_t idx) {
+    switch (kind) {
+    case ORACLE_BF16: return bf16_bits_value(((const uint16_t*)base)[idx]);
+    case ORACLE_FP16: return fp16_bits_value(((const uint16_t*)base)[idx]);
+    default: return ((const double*)base)[idx];
+    }
+}
+
+int oracle_decode(const uint16_t* bits, int64_t n, int kind, double* out) {
+    if (!bits || !out || n < 0) return -1;
+    if (kind != ORACLE_BF16 && kind != ORACLE_FP16) return -2;
+    for (int64_t t = 0; t < n; ++t) out[t] = elem(bits, kind, t);
+    return 0;
+}
+
+/* One output row: query i of head (b, h). `s` is scratch of at least N doubles. */
+static void attention_row(const void* q, const void* k, const void* v, int kind,
+                          int64_t N, int64_t H, int64_t d, int causal, double scale,
+                          int64_t b, int64_t h, int64_t i, double* s, double* o_row,
+                          double* lse_out) {
+    const int64_t q_off = ((b * N + i) * H + h) * d;
+    const int64_t n_keys = causal ? i + 1 : N;   /* keys j in [0, n_keys) are allowed */
+
+    /* Step 1: S[i, j] = scale * <q_i, k_j>. */
+    for (int64_t j = 0; j < n_keys; ++j) {
+        const int64_t k_off = ((b * N + j) * H + h) * d;
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c) dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);
+        s[j] = scale * dot;
+    }
+
+    /* Softmax pass 1: the row maximum. */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n_keys; ++j)
+        if (s[j] > m) m = s[j];
+
+    /* Softmax pass 2: the sum of exponentials relative to the maximum. */
+    double l = 0.0;
+    for (int64_t j = 0; j < n_keys; ++j) l += exp(s[j] - m);
+
+    /* Softmax pass 3: normalise, turning S[i, :] into P[i, :] in place. */
+    for (int64_t j = 0; j < n_keys; ++j) s[j] = exp(s[j] - m) / l;
+
+    /* Step 3: O[i, :] = P[i, :] V. */
+    for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+    for (int64_t j = 0; j < n_keys; ++j) {
+        const int64_t v_off = ((b * N + j) * H + h) * d;
+        for (int64_t c = 0; c < d; ++c) o_row[c] += s[j] * elem(v, kind, v_off + c);
+    }
+
+    *lse_out = m + log(l);
+}
+
+static int check_args(const void* q, const void* k, const void* v, int kind, int64_t B,
+                      int64_t H, int64_t N, int64_t d) {
+    if (!q || !k || !v) return -1;
+    if (kind != ORACLE_F64 && kind != ORACLE_BF16 && kind != ORACLE_FP16) return -2;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return -3;
+    return 0;
+}
+
+/* Full attention: o [B, N, H, d], lse [B, H, N]. */
+int oracle_attention(const void* q, const void* k, const void* v, int kind, int64_t B,
+                     int64_t H, int64_t N, int64_t d, int causal, double scale, double* o,
+                     double* lse) {
+    int rc = check_args(q, k, v, kind, B, H, N, d);
+    if (rc) return rc;
+    if (!o || !lse) return -1;
+    const int64_t rows = B * H * N;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc((size_t)N * sizeof(double));
+        if (!s) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 16)
+            for (int64_t r = 0; r < rows; ++r) {
+                /* r enumerates (b, h, i) with i fastest */
+                const int64_t i = r % N, h = (r / N) % H, b = r / (N * H);
+                attention_row(q, k, v, kind, N, H, d, causal, scale, b, h, i, s,
+                              o + ((b * N + i) * H + h) * d, lse + (b * H + h) * N + i);
+            }
+            free(s);
+        }
+    }
+    return failed ? -4 : 0;
+}
+
+/* Selected rows: rows[3t..3t+2] = (b, h, i); o_rows [nrows, d], lse_rows [nrows]. */
+int oracle_attention_rows(const void* q, const void* k, const void* v, int kind, int64_t B,
+                          int64_t H, int64_t N, int64_t d, int causal, double scale,
+                          const int64_t* rows, int64_t nrows, double* o_rows,
+                          double* lse_rows) {
+    int rc = check_args(q, k, v, kind, B, H, N, d);
+    if (rc) return rc;
+    if (!rows || !o_rows || !lse_rows || nrows < 0) return -1;
+    for (int64_t t = 0; t < nrows; ++t) {
+        const int64_t b = rows[3 * t], h = rows[3 * t + 1], i = rows[3 * t + 2];
+        if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= N) return -5;
+    }
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc((size_t)N * sizeof(double));
+        if (!s) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t t = 0; t < nrows; ++t)
+                attention_row(q, k, v, kind, N, H, d, causal, scale, rows[3 * t],
+                              rows[3 * t + 1], rows[3 * t + 2], s, o_rows + t * d,
+                              lse_rows + t);
+            free(s);
+        }
+    }
+    return failed ? -4 : 0;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

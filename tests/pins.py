@@ -1,0 +1,279 @@
+"""Pins for the attention oracle: checks against facts fixed by the pages and by mathematics.
+
+Each pin takes a loaded oracle library (``oracle.load()`` or a mutated build of the same
+source) and raises AssertionError when the oracle disagrees with the fact. None of them
+retypes the oracle's formula: they use closed forms, invariants, special cases with known
+answers, the method's tiled algorithm (a different evaluation order that the pages state
+reaches the same result), an independent arbitrary-precision evaluation without the max
+shift, and library conversions.
+
+Sources of the facts ("FlashAttention 优化原理与实现要点解析" unless noted):
+  §1  Attention(Q,K,V) = Softmax(QK^T/sqrt(d)) V; tiling does not change the result.
+  §4.1 softmax definition: rows of P are positive and sum to 1.
+  §4.2-§5 online softmax / tiled attention reach the exact softmax.
+  §7  causal: query i attends to keys j <= i.
+  "FlashAttention V2 核心原理与架构设计" §2.1: the element-wise online softmax.
+  "FlashAttention V2 核心原理与架构设计" §2.3: per-row statistics m and l are kept
+      (reported as LSE = m + ln l).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+
+
+def _rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _attn(lib, q, k, v, causal, scale):
+    return oracle.attention(q, k, v, causal, scale, lib=lib)
+
+
+# ---------------------------------------------------------------------------------------------
+def pin_decode_fp16(lib):
+    """fp16 decoding equals numpy's float16 -> float64 conversion for every bit pattern."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.decode(bits, "fp16", lib=lib)
+    want = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def pin_decode_bf16(lib):
+    """bf16 decoding equals torch's bfloat16 -> float64 conversion for every bit pattern."""
+    import torch
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.decode(bits, "bf16", lib=lib)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def pin_probability_rows(lib):
+    """With V = I (d = N), O[i, :] is row i of P: non-negative, summing to 1; causal rows
+    put exactly zero weight on keys j > i."""
+    N = 24
+    rng = _rng(11)
+    q = rng.standard_normal((2, N, 2, N))
+    k = rng.standard_normal((2, N, 2, N))
+    v = np.broadcast_to(np.eye(N)[None, :, None, :], (2, N, 2, N)).copy()
+    for causal in (False, True):
+        P, _ = _attn(lib, q, k, v, causal, 0.3)
+        assert (P >= 0).all()
+        assert np.abs(P.sum(axis=-1) - 1.0).max() < 1e-14
+        if causal:
+            upper = np.triu(np.ones((N, N), dtype=bool), 1)
+            assert (P.transpose(0, 2, 1, 3)[:, :, upper] == 0).all()
+        else:
+            assert (P > 0).all()
+
+
+def pin_zero_queries(lib):
+    """Q = 0 makes every score 0: O is the mean of the allowed V rows, LSE = ln(#keys)."""
+    B, N, H, d = 2, 37, 3, 8
+    rng = _rng(12)
+    q = np.zeros((B, N, H, d))
+    k = rng.standard_normal((B, N, H, d))
+    v = rng.standard_normal((B, N, H, d))
+    o, lse = _attn(lib, q, k, v, False, 0.125)
+    assert np.abs(o - v.mean(axis=1, keepdims=True)).max() < 1e-13
+    assert np.abs(lse - math.log(N)).max() < 1e-13
+    o, lse = _attn(lib, q, k, v, True, 0.125)
+    prefix_mean = np.cumsum(v, axis=1) / np.arange(1, N + 1)[None, :, None, None]
+    assert np.abs(o - prefix_mean).max() < 1e-13
+    assert np.abs(lse - np.log(np.arange(1, N + 1))[None, None, :]).max() < 1e-13
+
+
+def pin_constant_values(lib):
+    """V rows all equal to one vector c: O = c for every row, causal or not."""
+    B, N, H, d = 1, 29, 2, 16
+    rng = _rng(13)
+    q = 3 * rng.standard_normal((B, N, H, d))
+    k = rng.standard_normal((B, N, H, d))
+    c = rng.standard_normal((1, 1, H, d))
+    v = np.broadcast_to(c, (B, N, H, d)).copy()
+    for causal in (False, True):
+        o, _ = _attn(lib, q, k, v, causal, 0.25)
+        assert np.abs(o - c).max() < 1e-13
+
+
+def pin_causal_first_row(lib):
+    """Causal row 0 sees only key 0: O[0] = V[0] and LSE[0] = scale * <q_0, k_0>."""
+    B, N, H, d = 2, 17, 2, 8
+    rng = _rng(14)
+    q, k, v = (rng.standard_normal((B, N, H, d)) for _ in range(3))
+    scale = 0.35
+    o, lse = _attn(lib, q, k, v, True, scale)
+    assert np.abs(o[:, 0] - v[:, 0]).max() < 1e-15
+    want = scale * np.einsum("bhc,bhc->bh", q[:, 0], k[:, 0])
+    assert np.abs(lse[:, :, 0] - want).max() < 1e-13
+
+
+def pin_single_token(lib):
+    """N = 1: O = V and LSE = scale * <q, k>, causal or not."""
+    rng = _rng(15)
+    q, k, v = (rng.standard_normal((3, 1, 2, 5)) for _ in range(3))
+    for causal in (False, True):
+        o, lse = _attn(lib, q, k, v, causal, 0.7)
+        assert np.abs(o - v).max() < 1e-15
+        want = 0.7 * np.einsum("bnhc,bnhc->bhn", q, k)
+        assert np.abs(lse - want).max() < 1e-13
+
+
+def pin_two_key_closed_form(lib):
+    """One query, two keys with scores 0 and 1: p = (1, e) / (1 + e), so
+    O = (v0 + e v1) / (1 + e) and LSE = ln(1 + e)."""
+    q = np.array([[[[1.0]]], [[[1.0]]]]).reshape(1, 2, 1, 1)
+    k = np.array([0.0, 1.0]).reshape(1, 2, 1, 1)
+    v = np.array([2.0, -3.0]).reshape(1, 2, 1, 1)
+    o, lse = _attn(lib, q, k, v, False, 1.0)
+    e = math.e
+    assert abs(o[0, 0, 0, 0] - (2.0 - 3.0 * e) / (1 + e)) < 1e-15
+    assert abs(lse[0, 0, 0] - math.log(1 + e)) < 1e-15
+    # causal: row 0 sees only key 0 (score 0): O = v0, LSE = 0
+    o, lse = _attn(lib, q, k, v, True, 1.0)
+    assert o[0, 0, 0, 0] == 2.0 and lse[0, 0, 0] == 0.0
+    assert abs(o[0, 1, 0, 0] - (2.0 - 3.0 * e) / (1 + e)) < 1e-15
+
+
+def pin_key_shift(lib):
+    """Adding one vector w to every key row adds scale*<q_i, w> to row i's scores: O is
+    unchanged and LSE_i grows by exactly that amount (softmax is shift invariant)."""
+    B, N, H, d = 1, 40, 2, 8
+    rng = _rng(16)
+    q, k, v = (rng.standard_normal((B, N, H, d)) for _ in range(3))
+    w = rng.standard_normal((1, 1, H, d))
+    scale = 0.5
+    for causal in (False, True):
+        o0, l0 = _attn(lib, q, k, v, causal, scale)
+        o1, l1 = _attn(lib, q, k + w, v, causal, scale)
+        assert np.abs(o1 - o0).max() < 1e-12
+        shift = scale * np.einsum("bnhc,bnhc->bhn", q, np.broadcast_to(w, q.shape))
+        assert np.abs((l1 - l0) - shift).max() < 1e-12
+
+
+def pin_kv_permutation(lib):
+    """Non-causal attention is invariant under one permutation applied to the rows of K
+    and V together."""
+    B, N, H, d = 2, 33, 2, 8
+    rng = _rng(17)
+    q, k, v = (rng.standard_normal((B, N, H, d)) for _ in range(3))
+    perm = rng.permutation(N)
+    o0, l0 = _attn(lib, q, k, v, False, 0.4)
+    o1, l1 = _attn(lib, q, k[:, perm], v[:, perm], False, 0.4)
+    assert np.abs(o1 - o0).max() < 1e-13
+    assert np.abs(l1 - l0).max() < 1e-13
+
+
+def _brute_force_mp(q, k, v, causal, scale):
+    """sum_j e^{s_j} v_j / sum_j e^{s_j} in 60-digit arithmetic, no max shift."""
+    import mpmath
+    mp = mpmath.mp.clone()
+    mp.dps = 60
+    B, N, H, d = q.shape
+    o = np.zeros((B, N, H, d))
+    lse = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                js = range(i + 1) if causal else range(N)
+                ws = []
+                for j in js:
+                    s = mp.mpf(0)
+                    for c in range(d):
+                        s += mp.mpf(float(q[b, i, h, c])) * mp.mpf(float(k[b, j, h, c]))
+                    ws.append(mp.exp(mp.mpf(scale) * s))
+                den = mp.fsum(ws)
+                for c in range(d):
+                    num = mp.fsum(wj * mp.mpf(float(v[b, j, h, c])) for wj, j in zip(ws, js))
+                    o[b, i, h, c] = float(num / den)
+                lse[b, h, i] = float(mp.log(den))
+    return o, lse
+
+
+def pin_brute_force_small(lib):
+    """N <= 16, several heads and batches: equals an independent 60-digit evaluation of the
+    definition without the max shift, both masks, moderate logits."""
+    rng = _rng(18)
+    for (B, N, H, d) in [(1, 1, 1, 4), (2, 7, 3, 5), (1, 16, 2, 8)]:
+        q, k, v = (rng.standard_normal((B, N, H, d)) for _ in range(3))
+        for causal in (False, True):
+            o, lse = _attn(lib, q, k, v, causal, 0.6)
+            ob, lb = _brute_force_mp(q, k, v, causal, 0.6)
+            assert np.abs(o - ob).max() < 1e-12
+            assert np.abs(lse - lb).max() < 1e-12
+
+
+def pin_brute_force_large_logits(lib):
+    """Scores in the thousands (e^s overflows float64 without the max shift): the oracle
+    stays finite and matches the 60-digit evaluation, which needs no shift."""
+    rng = _rng(19)
+    B, N, H, d = 1, 12, 2, 4
+    q = 40 * rng.standard_normal((B, N, H, d))
+    k = 40 * rng.standard_normal((B, N, H, d))
+    v = rng.standard_normal((B, N, H, d))
+    for causal in (False, True):
+        o, lse = _attn(lib, q, k, v, causal, 0.5)
+        ob, lb = _brute_force_mp(q, k, v, causal, 0.5)
+        assert np.isfinite(o).all() and np.isfinite(lse).all()
+        assert np.abs(o - ob).max() < 1e-12
+        assert (np.abs(lse - lb) / np.maximum(1.0, np.abs(lb))).max() < 1e-13
+
+
+def pin_tiled_algorithm(lib):
+    """The pages' tiled online-softmax algorithm (Q blocks outer, K/V blocks inner, causal
+    block skip, normalisation at the end) reaches the plain definition: several block shapes,
+    ragged tails, both masks."""
+    rng = _rng(20)
+    N, d = 45, 8
+    q, k, v = (rng.standard_normal((1, N, 1, d)) for _ in range(3))
+    for causal in (False, True):
+        o, lse = _attn(lib, q, k, v, causal, 0.4)
+        for Br, Bc in [(1, 1), (8, 8), (16, 7), (45, 45), (64, 16)]:
+            ot, lt = oracle.blockwise_attention(q[0, :, 0], k[0, :, 0], v[0, :, 0], Br, Bc,
+                                                causal, 0.4)
+            assert np.abs(ot - o[0, :, 0]).max() < 1e-12
+            assert np.abs(lt - lse[0, 0]).max() < 1e-12
+
+
+def pin_torch_math_sdpa(lib):
+    """Third opinion: torch's math scaled_dot_product_attention in float64 on the CPU."""
+    import torch
+    rng = _rng(21)
+    B, N, H, d = 2, 50, 3, 16
+    q, k, v = (rng.standard_normal((B, N, H, d)) for _ in range(3))
+    for causal in (False, True):
+        o, _ = _attn(lib, q, k, v, causal, 0.3)
+        t = [torch.from_numpy(x).permute(0, 2, 1, 3) for x in (q, k, v)]
+        ref = torch.nn.functional.scaled_dot_product_attention(*t, is_causal=causal, scale=0.3)
+        assert np.abs(o - ref.permute(0, 2, 1, 3).numpy()).max() < 1e-12
+
+
+def pin_dtype_inputs(lib):
+    """Bit-pattern inputs give the same result as their exactly decoded values, for both
+    storage types, and the selected-rows entry point matches the full one."""
+    from io_aware_attention_fa2_gb300.inputs import make_qkv
+    for dtype in ("bf16", "fp16"):
+        qb, kb, vb = make_qkv(1, 2, 20, 8, dtype, seed=7, q_scale=2.0)
+        o_bits, l_bits = oracle.attention(qb, kb, vb, True, 0.3, dtype=dtype, lib=lib)
+        dec = [oracle.decode(x, dtype, lib=lib) for x in (qb, kb, vb)]
+        o_f, l_f = _attn(lib, *dec, True, 0.3)
+        assert np.array_equal(o_bits, o_f) and np.array_equal(l_bits, l_f)
+        rows = np.array([[0, 1, 19], [0, 0, 0], [0, 1, 7]])
+        o_r, l_r = oracle.attention_rows(qb, kb, vb, rows, True, 0.3, dtype=dtype, lib=lib)
+        for t, (b, h, i) in enumerate(rows):
+            assert np.array_equal(o_r[t], o_bits[b, i, h]) and l_r[t] == l_bits[b, h, i]
+
+
+ALL_PINS = [
+    pin_decode_fp16, pin_decode_bf16, pin_probability_rows, pin_zero_queries,
+    pin_constant_values, pin_causal_first_row, pin_single_token, pin_two_key_closed_form,
+    pin_key_shift, pin_kv_permutation, pin_brute_force_small, pin_brute_force_large_logits,
+    pin_tiled_algorithm, pin_torch_math_sdpa, pin_dtype_inputs,
+]

@@ -1,0 +1,60 @@
+"""Plant plausible mistakes in a copy of the oracle's C source and check that the pins catch
+every one of them (CPU only). The real source is never modified."""
+import os
+
+import pytest
+
+import oracle
+from pins import ALL_PINS
+
+# (name, exact snippet of attn_oracle.c, replacement)
+MUTANTS = [
+    ("dropped_max_shift", "l += exp(s[j] - m);", "l += exp(s[j]);"),
+    ("normalise_without_shift", "s[j] = exp(s[j] - m) / l;", "s[j] = exp(s[j]) / l;"),
+    ("wrong_sign_in_exp", "s[j] = exp(s[j] - m) / l;", "s[j] = exp(m - s[j]) / l;"),
+    ("transposed_q_k", "dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);",
+     "dot += elem(k, kind, q_off + c) * elem(q, kind, k_off + c);"),
+    ("query_row_for_value", "const int64_t v_off = ((b * N + j) * H + h) * d;",
+     "const int64_t v_off = ((b * N + i) * H + h) * d;"),
+    ("causal_excludes_diagonal", "causal ? i + 1 : N;", "causal ? i : N;"),
+    ("causal_off_by_one_extra", "causal ? i + 1 : N;", "causal ? (i + 2 < N ? i + 2 : N) : N;"),
+    ("scale_dropped", "s[j] = scale * dot;", "s[j] = dot;"),
+    ("scale_squared", "s[j] = scale * dot;", "s[j] = scale * scale * dot;"),
+    ("lse_without_max", "*lse_out = m + log(l);", "*lse_out = log(l);"),
+    ("lse_base2", "*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
+    ("no_normalisation", "s[j] = exp(s[j] - m) / l;", "s[j] = exp(s[j] - m);"),
+    ("head_index_ignored", "const int64_t k_off = ((b * N + j) * H + h) * d;",
+     "const int64_t k_off = ((b * N + j) * H + 0) * d;"),
+    ("batch_index_ignored", "const int64_t q_off = ((b * N + i) * H + h) * d;",
+     "const int64_t q_off = ((0 * N + i) * H + h) * d;"),
+    ("max_over_prefix_only", "for (int64_t j = 0; j < n_keys; ++j)\n        if (s[j] > m)",
+     "for (int64_t j = 0; j < n_keys / 2; ++j)\n        if (s[j] > m)"),
+    ("fp16_bias_wrong", "ldexp((double)(1024 + mant), expo - 25)",
+     "ldexp((double)(1024 + mant), expo - 24)"),
+    ("fp16_subnormal_wrong", "ldexp((double)mant, -24)", "ldexp((double)mant, -25)"),
+    ("bf16_shift_wrong", "(uint32_t)bits << 16", "(uint32_t)bits << 15"),
+    ("lse_stride_wrong", "lse + (b * H + h) * N + i", "lse + (b * H + h) * N + 0"),
+]
+
+
+def test_real_source_passes_every_pin(oracle_lib):
+    pytest.importorskip("mpmath")
+    for pin in ALL_PINS:
+        pin(oracle_lib)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, tmp_path):
+    pytest.importorskip("mpmath")
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, "mutation site must be unique: %r" % old
+    mutated = tmp_path / ("oracle_%s.c" % name)
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.load(oracle.compile_library(str(mutated), str(tmp_path / ("lib_%s.so" % name))))
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, RuntimeError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, "no pin catches the mutant %s" % name
