@@ -1,0 +1,385 @@
+"""Benchmark of the fused attention forward on GB300.
+
+Default workload: B=2, H=16, N=8192, d=128, bf16, causal (the long-sequence headline case).
+One step = one fa_fwd call over the whole batch. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+* value: attention-forward TFLOP/s, FLOPs = 4*B*H*N^2*d (halved when causal), inputs resident
+  in HBM, kernel time from CUDA events on the launching stream, L2 flushed (256 MiB write)
+  before every timed step.
+* e2e: the same metric through the user API with host buffers: pinned host -> device copies of
+  Q, K, V, the kernel, and device -> host copies of O and LSE inside every timed step.
+* roofline: tensor-bound; achieved = metric FLOPs per launch / mean launch time, peak = the
+  measured dense bf16 matmul rate of this GPU type (burst), frac = achieved / peak.
+* cpu_baseline: the fp64 oracle timed on this host's cores on a bounded sample of the same
+  workload (uniformly sampled query rows), in the same unit.
+* --gpus N > 1 (under torchrun): N independent replicas, one per GPU, no collective on the
+  data path; value = all FLOPs / max-over-ranks time ("weak" scaling).
+* --impl reference: the oracle, timed on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from io_aware_attention_fa2_gb300.inputs import WORKLOADS, make_workload, sample_rows  # noqa
+
+DEFAULT_WORKLOAD = "n8k_d128_causal"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["io_aware_attention_fa2_gb300/csrc/fa_fwd_kernel.cu",
+                  "io_aware_attention_fa2_gb300/csrc/ptx_sm103.cuh",
+                  "io_aware_attention_fa2_gb300/csrc/fa_internal.h"]
+
+
+def metric_flops(w) -> float:
+    f = 4.0 * w.B * w.H * w.N * w.N * w.d
+    return f / 2 if w.causal else f
+
+
+def algorithmic_bytes(w) -> int:
+    """Q, K, V read once, O written once (2 bytes each), LSE written once (4 bytes)."""
+    return 4 * w.B * w.H * w.N * w.d * 2 + w.B * w.H * w.N * 4
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, 0.0, "fallback"
+
+
+def traffic_record(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel."""
+    path = os.path.join(ROOT, "profiles", "fa_fwd_%s_dram.txt" % workload)
+    try:
+        rec = {}
+        with open(path) as f:
+            for line in f:
+                if "=" in line and not line.startswith("#"):
+                    key, val = line.split("=", 1)
+                    rec[key.strip()] = val.strip()
+        if rec.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return int(float(rec["dram_bytes_per_launch"]))
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return None
+        self.out.flush()
+        with open(self.out.name) as f:
+            rows = [r.split(",") for r in f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = max(float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower() == "active"})
+        loaded = [s for s in sm if s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cpu_baseline(w, qb, kb, vb, target_s: float = 15.0, min_rows: int = 64):
+    """Time the oracle on uniformly sampled query rows of the workload (bounded CPU work)."""
+    import oracle
+    lib = oracle.load()
+    total_rows = w.B * w.H * w.N
+    rng = np.random.Generator(np.random.PCG64(w.seed + 11))
+
+    def pick(n):
+        flat = rng.choice(total_rows, size=min(n, total_rows), replace=False)
+        i = flat % w.N
+        h = (flat // w.N) % w.H
+        b = flat // (w.N * w.H)
+        return np.stack([b, h, i], axis=1)
+
+    # calibrate on a small sample, then size the run to about target_s seconds
+    rows = pick(min_rows)
+    t0 = time.perf_counter()
+    oracle.attention_rows(qb, kb, vb, rows, w.causal, w.scale, dtype=w.dtype, lib=lib)
+    dt = time.perf_counter() - t0
+    n = int(min(total_rows, max(min_rows, min_rows * target_s / max(dt, 1e-3))))
+    rows = pick(n)
+    t0 = time.perf_counter()
+    oracle.attention_rows(qb, kb, vb, rows, w.causal, w.scale, dtype=w.dtype, lib=lib)
+    dt = time.perf_counter() - t0
+    flops = metric_flops(w) * (len(rows) / total_rows)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(lib),
+            "kind": "oracle",
+            "sample": "%d uniformly sampled query rows of %d (%.2f%%) in %.1f s; FLOPs "
+                      "pro rata of the workload's metric FLOPs" %
+                      (len(rows), total_rows, 100.0 * len(rows) / total_rows, dt),
+            "seconds": dt}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    qb, kb, vb = make_workload(w)
+    vals = []
+    cb = None
+    for _ in range(args.warmup + args.steps):
+        cb = cpu_baseline(w, qb, kb, vb, target_s=args.ref_step_seconds, min_rows=32)
+        vals.append(cb["value"])
+    vals = vals[args.warmup:]
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": "attn fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * cb["seconds"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe()},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cb["cores"],
+                         "kind": "oracle", "sample": cb["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from io_aware_attention_fa2_gb300 import binding
+    from io_aware_attention_fa2_gb300 import build as fa_build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(binding.library_path()):
+        fa_build.build()
+    if world > 1:
+        dist.barrier()
+    binding.load_library()
+
+    qb, kb, vb = make_workload(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    host = [torch.from_numpy(x.view(np.int16)).view(tdt).pin_memory() for x in (qb, kb, vb)]
+    q, k, v = (t.to(dev) for t in host)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # parity on sampled rows before timing (rank 0)
+    parity = None
+    if rank == 0 and not args.no_check:
+        import oracle
+        binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+        if binding.device_error(stream) != 0:
+            raise RuntimeError("kernel wait timed out")
+        rows = sample_rows(w.B, w.H, w.N, 8, seed=w.seed + 5)
+        o_ref, l_ref = oracle.attention_rows(qb, kb, vb, rows, w.causal, w.scale,
+                                             dtype=w.dtype)
+        idx = [torch.from_numpy(rows[:, c]).to(dev) for c in range(3)]
+        og = o[idx[0], idx[2], idx[1]].double().cpu().numpy()
+        lg = lse[idx[0], idx[1], idx[2]].double().cpu().numpy()
+        d_o = og - o_ref
+        parity = {"rows": int(len(rows)), "max_abs_o": float(np.abs(d_o).max()),
+                  "rel_l2_o": float(np.linalg.norm(d_o) / np.linalg.norm(o_ref)),
+                  "max_abs_lse": float(np.abs(lg - l_ref).max())}
+        if not (parity["max_abs_o"] <= 1e-2 and parity["rel_l2_o"] <= 5e-3
+                and parity["max_abs_lse"] <= 1e-3):
+            print(json.dumps({"error": "parity failed", "parity": parity}), flush=True)
+            return 3
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+        if world > 1:
+            dist.barrier()
+    if binding.device_error(stream) != 0:
+        raise RuntimeError("kernel wait timed out during timing")
+    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = statistics.mean(per_step_ms)
+    total_ms = sum(per_step_ms)
+
+    # end to end through the user API with host buffers (pinned), copies in the timed region
+    o_host = torch.empty(q.shape, dtype=tdt, pin_memory=True)
+    l_host = torch.empty((w.B, w.H, w.N), dtype=torch.float32, pin_memory=True)
+
+    def e2e_step():
+        binding.attention_forward(*host, causal=w.causal, scale=w.scale, out=o_host,
+                                  lse=l_host, stream=stream, device=dev)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ms = 1e3 * (time.perf_counter() - t0) / args.steps
+
+    flops = metric_flops(w)
+    stats = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(stats, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = (float(x) for x in stats.cpu())
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    if rank == 0:
+        peak, peak_sus, peak_src = measured_peaks()
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        line = {
+            "metric": "attn fwd TFLOP/s (causal N=8K d=128 headline)" if w.name ==
+            DEFAULT_WORKLOAD else "attn fwd TFLOP/s",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "shape": w.describe(),
+                       "l2": "256 MiB flush write before every timed step; per-step CUDA "
+                             "events around the kernel only",
+                       "parallelism": "replicas x%d" % world},
+            "pct_of_peak": 100.0 * achieved / peak,
+            "peak_denominator": "%s bf16 dense %.1f TFLOP/s" % (peak_src, peak),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": "%s (burst)" % peak_src,
+                         "traffic": traffic_record(w.name),
+                         "algorithmic_bytes": algorithmic_bytes(w)},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host),
+                    "d2h_bytes_per_step": o_host.numel() * 2 + l_host.numel() * 4,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "kernel_ms": {"mean": kernel_ms, "min": min(per_step_ms),
+                          "max": max(per_step_ms)},
+            "wall_s_timed_region": t_wall,
+            "clocks": clocks.summary(),
+            "parity": parity,
+        }
+        if peak_sus:
+            line["roofline"]["frac_of_sustained"] = achieved / peak_sus
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = {k: v for k, v in
+                                    cpu_baseline(w, qb, kb, vb, args.cpu_seconds).items()
+                                    if k != "seconds"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-check", action="store_true", help="skip the sampled parity check")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=5.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

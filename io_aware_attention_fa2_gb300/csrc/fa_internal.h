@@ -1,0 +1,40 @@
+// fa_internal.h -- declarations shared by the two translation units of the CUDA library
+// (fa_api.cpp: argument checks, tensor maps, C ABI; fa_fwd_kernel.cu: kernels and launch).
+// Not part of the public ABI (that is include/fa.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Tile shape of one work unit: BLOCK_M query rows against BLOCK_N keys per K/V tile.
+constexpr int BLOCK_M = 128;
+constexpr int BLOCK_N = 128;
+// A TMA box is BOX_ROWS tokens x BOX_COLS 16-bit elements (one 128-byte swizzle span per row).
+constexpr int BOX_ROWS = 128;
+constexpr int BOX_COLS = 64;
+
+struct FwdParams {
+  CUtensorMap tm_q;   // [B, N, H, d] viewed as 4-D (d, H, N, B); box (64, 1, 128, 1)
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  void* o;            // [B, N, H, d], same storage type as q
+  float* lse;         // [B, H, N]
+  int B, H, N, d;
+  int causal;
+  int fp16;           // 0: bf16, 1: fp16
+  float scale_log2;   // scale * log2(e)
+};
+
+// Enqueue the forward kernel. Returns a CUDA error (cudaSuccess when enqueued).
+cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
+
+// Dynamic shared memory the forward kernel needs for head dimension d.
+size_t fwd_smem_bytes(int d);
+
+// Device error word of the current device: read (after synchronising `stream`) and clear.
+cudaError_t read_and_clear_device_error(cudaStream_t stream, int* value);
+
+}  // namespace fa

@@ -1,0 +1,56 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI on bit-exact copies of
+the seeded inputs, and compare with the oracle.
+
+Tolerances (fp64 oracle, unrounded, against the kernel's bf16/fp16 output):
+  max |dO| <= 1e-2, ||dO||_2 / ||O_ref||_2 <= 5e-3, max |dLSE| <= 1e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+MAX_ABS_O = 1e-2
+REL_L2_O = 5e-3
+MAX_ABS_LSE = 1e-3
+
+
+def to_device(bits: np.ndarray, dtype: str):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    t = t.view(torch.bfloat16 if dtype == "bf16" else torch.float16)
+    return t.cuda()
+
+
+def run_gpu(qb, kb, vb, dtype: str, causal: bool, scale: float, check_error: bool = True):
+    """fa_fwd on the GPU. Returns (o float64 [B,N,H,d], lse float64 [B,H,N]) as numpy."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    q, k, v = (to_device(x, dtype) for x in (qb, kb, vb))
+    B, N, H, d = q.shape
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=q.device)
+    binding.fa_fwd(q, k, v, o, lse, causal, scale)
+    if check_error:
+        assert binding.device_error() == 0, "a kernel wait ran out"
+    torch.cuda.synchronize()
+    return o.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def compare(o, lse, o_ref, lse_ref):
+    """Error statistics of (o, lse) against the oracle."""
+    d_o = o - o_ref
+    return {
+        "max_abs_o": float(np.abs(d_o).max()) if d_o.size else 0.0,
+        "rel_l2_o": float(np.linalg.norm(d_o) / max(np.linalg.norm(o_ref), 1e-300)),
+        "max_abs_lse": float(np.abs(lse - lse_ref).max()) if lse.size else 0.0,
+        "finite": bool(np.isfinite(o).all() and np.isfinite(lse).all()),
+    }
+
+
+def assert_close(o, lse, o_ref, lse_ref, what: str = ""):
+    st = compare(o, lse, o_ref, lse_ref)
+    assert st["finite"], "non-finite output %s" % what
+    assert st["max_abs_o"] <= MAX_ABS_O, (what, st)
+    assert st["rel_l2_o"] <= REL_L2_O, (what, st)
+    assert st["max_abs_lse"] <= MAX_ABS_LSE, (what, st)
+    return st
