@@ -150,59 +150,84 @@ def dist_env():
     return rank, world, local
 
 
-def cpu_baseline(w, qb, kb, vb, target_s: float = 15.0, min_rows: int = 64):
-    """Time the oracle on uniformly sampled query rows of the workload (bounded CPU work)."""
-    import oracle
-    lib = oracle.load()
-    total_rows = w.B * w.H * w.N
-    rng = np.random.Generator(np.random.PCG64(w.seed + 11))
+class OracleSampler:
+    """Times the oracle on uniformly sampled query rows of a workload (bounded CPU work)."""
 
-    def pick(n):
-        flat = rng.choice(total_rows, size=min(n, total_rows), replace=False)
-        i = flat % w.N
-        h = (flat // w.N) % w.H
-        b = flat // (w.N * w.H)
-        return np.stack([b, h, i], axis=1)
+    def __init__(self, w, qb, kb, vb):
+        import oracle
+        self.oracle = oracle
+        self.lib = oracle.load()
+        self.w, self.qb, self.kb, self.vb = w, qb, kb, vb
+        self.total_rows = w.B * w.H * w.N
+        self.rng = np.random.Generator(np.random.PCG64(w.seed + 11))
+        self.rows_per_s = None
 
-    # calibrate on a small sample, then size the run to about target_s seconds
-    rows = pick(min_rows)
-    t0 = time.perf_counter()
-    oracle.attention_rows(qb, kb, vb, rows, w.causal, w.scale, dtype=w.dtype, lib=lib)
-    dt = time.perf_counter() - t0
-    n = int(min(total_rows, max(min_rows, min_rows * target_s / max(dt, 1e-3))))
-    rows = pick(n)
-    t0 = time.perf_counter()
-    oracle.attention_rows(qb, kb, vb, rows, w.causal, w.scale, dtype=w.dtype, lib=lib)
-    dt = time.perf_counter() - t0
-    flops = metric_flops(w) * (len(rows) / total_rows)
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(lib),
+    def pick(self, n):
+        w = self.w
+        flat = self.rng.choice(self.total_rows, size=min(n, self.total_rows), replace=False)
+        return np.stack([flat // (w.N * w.H), (flat // w.N) % w.H, flat % w.N], axis=1)
+
+    def run(self, n_rows):
+        """(metric FLOPs of the sampled rows, seconds, rows)."""
+        w = self.w
+        rows = self.pick(n_rows)
+        t0 = time.perf_counter()
+        self.oracle.attention_rows(self.qb, self.kb, self.vb, rows, w.causal, w.scale,
+                                   dtype=w.dtype, lib=self.lib)
+        dt = time.perf_counter() - t0
+        return metric_flops(w) * (len(rows) / self.total_rows), dt, len(rows)
+
+    def rows_for(self, seconds, min_rows=16):
+        if self.rows_per_s is None:
+            n = 64
+            _, dt, n = self.run(n)
+            self.rows_per_s = n / max(dt, 1e-4)
+        return int(min(self.total_rows, max(min_rows, self.rows_per_s * seconds)))
+
+    def cores(self):
+        return self.oracle.max_threads(self.lib)
+
+
+def cpu_baseline(w, qb, kb, vb, target_s: float = 15.0):
+    s = OracleSampler(w, qb, kb, vb)
+    flops, dt, n = s.run(s.rows_for(target_s))
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": s.cores(),
             "kind": "oracle",
-            "sample": "%d uniformly sampled query rows of %d (%.2f%%) in %.1f s; FLOPs "
-                      "pro rata of the workload's metric FLOPs" %
-                      (len(rows), total_rows, 100.0 * len(rows) / total_rows, dt),
-            "seconds": dt}
+            "sample": "%d uniformly sampled query rows of %d (%.2f%%) in %.1f s; FLOPs pro "
+                      "rata of the workload's metric FLOPs" %
+                      (n, s.total_rows, 100.0 * n / s.total_rows, dt)}
 
 
 def run_reference(args, w):
+    """The oracle as it stands, timed on the host cores: every step is a bounded sample of the
+    workload (uniform query rows), sized so that warm-up + timed steps take about
+    --ref-total-seconds altogether."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     qb, kb, vb = make_workload(w)
-    vals = []
-    cb = None
-    for _ in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, qb, kb, vb, target_s=args.ref_step_seconds, min_rows=32)
-        vals.append(cb["value"])
-    vals = vals[args.warmup:]
-    value = statistics.mean(vals)
+    s = OracleSampler(w, qb, kb, vb)
+    per_step = args.ref_total_seconds / (args.steps + args.warmup)
+    n_rows = s.rows_for(per_step)
+    for _ in range(args.warmup):
+        s.run(n_rows)
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f, dt, n = s.run(n_rows)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    sample = ("%d uniformly sampled query rows of %d per step (%.3f%% of the workload); FLOPs "
+              "pro rata of the workload's metric FLOPs" % (n, s.total_rows,
+                                                           100.0 * n / s.total_rows))
     line = {
         "impl": "reference", "metric": "attn fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * cb["seconds"], "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "shape": w.describe()},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cb["cores"],
-                         "kind": "oracle", "sample": cb["sample"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": s.cores(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -353,8 +378,7 @@ def run_gpu(args, w):
             line["roofline"]["frac_of_sustained"] = achieved / peak_sus
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = {k: v for k, v in
-                                    cpu_baseline(w, qb, kb, vb, args.cpu_seconds).items()
-                                    if k != "seconds"}
+                                    cpu_baseline(w, qb, kb, vb, args.cpu_seconds).items()}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -364,14 +388,14 @@ def run_gpu(args, w):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-check", action="store_true", help="skip the sampled parity check")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--ref-step-seconds", type=float, default=5.0)
+    ap.add_argument("--ref-total-seconds", type=float, default=120.0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
