@@ -103,10 +103,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return FA_ERR_SHAPE;
   if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
   if (!isfinite(scale)) return FA_ERR_SCALE;
-  // Sizes: elements must fit int64; the grid is (B*H, ceil(N/128)) and TMA coordinates are
-  // 32-bit, so B*H < 2^31 and ceil(N/128) <= 65535.
+  // Sizes: elements must fit int64; the grid is one CTA per (b, h, 256-row Q block), at most
+  // 2^31 - 1 CTAs.
   const uint64_t bh = (uint64_t)B * (uint64_t)H;
-  if (bh >= (1ull << 31) || (uint64_t)(N + fa::BLOCK_M - 1) / fa::BLOCK_M > 65535ull)
+  if (bh >= (1ull << 31) || bh * (uint64_t)((N + 255) / 256) >= (1ull << 31))
     return FA_ERR_SHAPE;
   const uint64_t elems = bh * (uint64_t)N * (uint64_t)d;
   if (elems > (1ull << 62) / 2) return FA_ERR_SHAPE;

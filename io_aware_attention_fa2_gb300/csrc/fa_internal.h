@@ -34,6 +34,9 @@ cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
 // Dynamic shared memory the forward kernel needs for head dimension d.
 size_t fwd_smem_bytes(int d);
 
+// Number of CTAs (one per 256-row Q block of every (b, h)) the forward kernel launches.
+long long fwd_num_ctas(int B, int H, int N);
+
 // Device error word of the current device: read (after synchronising `stream`) and clear.
 cudaError_t read_and_clear_device_error(cudaStream_t stream, int* value);
 

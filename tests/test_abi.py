@@ -59,7 +59,7 @@ def test_host_side_argument_checks(lib):
     assert _call(lib, H=-1) == FA_ERR_SHAPE
     for d in (0, 32, 96, 256):
         assert _call(lib, d=d) == FA_ERR_SHAPE
-    assert _call(lib, N=65536 * 128) == FA_ERR_SHAPE          # more than 65535 Q tiles
+    assert _call(lib, B=1 << 12, H=1 << 8, N=1 << 20) == FA_ERR_SHAPE   # >= 2^31 CTAs
     assert _call(lib, B=1 << 16, H=1 << 15) == FA_ERR_SHAPE   # B*H >= 2^31
     assert _call(lib, dtype=2) == FA_ERR_DTYPE
     assert _call(lib, scale=float("nan")) == FA_ERR_SCALE
