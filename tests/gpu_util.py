@@ -3,6 +3,11 @@ the seeded inputs, and compare with the oracle.
 
 Tolerances (fp64 oracle, unrounded, against the kernel's bf16/fp16 output):
   max |dO| <= 1e-2, ||dO||_2 / ||O_ref||_2 <= 5e-3, max |dLSE| <= 1e-3.
+
+Cases outside the stated workloads can make attention so peaked that |O| reaches 4 or more,
+where rounding O to bf16 alone moves it by up to half an ulp (2^-6 = 0.0156 at [4, 8)). For
+those, ``out_dtype`` switches the absolute bound to an element-wise one derived from that
+arithmetic: |dO| <= 1e-2 + half an ulp of the output type at |O_ref|.
 """
 from __future__ import annotations
 
@@ -47,10 +52,21 @@ def compare(o, lse, o_ref, lse_ref):
     }
 
 
-def assert_close(o, lse, o_ref, lse_ref, what: str = ""):
+def half_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Half the spacing of bf16 (8 significant bits) or fp16 (11) numbers around |x|."""
+    bits = 8 if dtype == "bf16" else 11
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -14)))
+    return 0.5 * 2.0 ** (e - (bits - 1))
+
+
+def assert_close(o, lse, o_ref, lse_ref, what: str = "", out_dtype: str | None = None):
     st = compare(o, lse, o_ref, lse_ref)
     assert st["finite"], "non-finite output %s" % what
-    assert st["max_abs_o"] <= MAX_ABS_O, (what, st)
+    if out_dtype is None:
+        assert st["max_abs_o"] <= MAX_ABS_O, (what, st)
+    else:
+        excess = np.abs(o - o_ref) - (MAX_ABS_O + half_ulp(o_ref, out_dtype))
+        assert excess.max() <= 0, (what, st, float(excess.max()))
     assert st["rel_l2_o"] <= REL_L2_O, (what, st)
     assert st["max_abs_lse"] <= MAX_ABS_LSE, (what, st)
     return st
