@@ -43,6 +43,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "fa_internal.h"
 #include "ptx_sm103.cuh"
 
@@ -119,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
-                  float* __restrict__ lse_ptr, int H, int N, int causal, float scale_log2) {
+                  float* __restrict__ lse_ptr, int H, int N, int causal, float scale_log2,
+                  int heads_per_group) {
   using L = SmemLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_base_slot;
@@ -134,11 +137,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // Work unit from a 1-D grid: Q blocks of one (b, h) are consecutive, so the CTAs in flight
-  // share few heads and their K/V re-reads hit L2. Causal units are dispatched longest first.
+  // Work unit from a 1-D grid. Heads are taken in groups of `heads_per_group` (sized on the
+  // host so that a group's K and V stay resident in L2); within a group, units go Q block by
+  // Q block across the group's heads, longest (causal) block first, so the CTAs in flight share
+  // few heads and the long blocks start early.
   const int num_qblk = (N + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M);
-  const int bh = static_cast<int>(blockIdx.x) / num_qblk;
-  const int r = static_cast<int>(blockIdx.x) % num_qblk;
+  const int num_bh = gridDim.x / num_qblk;
+  const int group_units = heads_per_group * num_qblk;
+  const int g = static_cast<int>(blockIdx.x) / group_units;
+  const int rem = static_cast<int>(blockIdx.x) % group_units;
+  const int g_size = min(heads_per_group, num_bh - g * heads_per_group);
+  const int bh = g * heads_per_group + rem % g_size;
+  const int r = rem / g_size;
   const int qblk = causal ? num_qblk - 1 - r : r;
   const int b = bh / H, h = bh % H;
   const int num_kv_total = (N + BLOCK_N - 1) / BLOCK_N;
@@ -332,8 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int k0 = j * BLOCK_N;
       if (!scale_pos) {
+        // Non-positive scale: scale first, so that the maximum below is the maximum of the
+        // scaled scores.
 #pragma unroll
-        for (int t = 0; t < BLOCK_N; ++t) s[t] *= scale_log2;
+        for (int t = 0; t < BLOCK_N; t += 2)
+          ptx::mul2(s[t], s[t + 1], s[t], s[t + 1], scale_log2, scale_log2);
       }
       if ((causal && k0 + BLOCK_N - 1 > qt * BLOCK_M) || k0 + BLOCK_N > N) {
         const int lim = (causal ? min(q_idx + 1, N) : N) - k0;   // keys k0 + [0, lim) allowed
@@ -341,13 +354,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < BLOCK_N; ++t)
           if (t >= lim) s[t] = -INFINITY;
       }
-      float mt0 = -INFINITY, mt1 = -INFINITY;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int t = 0; t < BLOCK_N; t += 2) {
-        mt0 = fmaxf(mt0, s[t]);
-        mt1 = fmaxf(mt1, s[t + 1]);
+      for (int t = 0; t < BLOCK_N; t += 8) {
+        mx[0] = ptx::max3(mx[0], s[t + 0], s[t + 1]);
+        mx[1] = ptx::max3(mx[1], s[t + 2], s[t + 3]);
+        mx[2] = ptx::max3(mx[2], s[t + 4], s[t + 5]);
+        mx[3] = ptx::max3(mx[3], s[t + 6], s[t + 7]);
       }
-      const float mt = fmaxf(mt0, mt1);
+      const float mt = fmaxf(ptx::max3(mx[0], mx[1], mx[2]), mx[3]);
       const float m_tile = scale_pos ? mt * scale_log2 : mt;
       float alpha = 1.f;
       const bool rescale = __any_sync(0xffffffffu, m_tile > m + kRescaleLog2);
@@ -363,22 +378,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P_x(j) = 2^(scaled score - m) -> TMEM over the first 64 columns of S_x, 32 keys (16
       // columns) at a time: column c holds keys 2c (low half) and 2c + 1 (high half), rounded
       // to the input type.
+      // exponent argument: s * scale_log2 - m_use (positive scale, folded into one FMA) or
+      // s - m_use (s already scaled)
       float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
       for (int c = 0; c < BLOCK_N / 32; ++c) {
         uint32_t pr[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-          float p0, p1;
-          if (scale_pos) {
-            p0 = ptx::exp2_approx(fmaf(s[32 * c + 2 * t], scale_log2, -m_use));
-            p1 = ptx::exp2_approx(fmaf(s[32 * c + 2 * t + 1], scale_log2, -m_use));
-          } else {
-            p0 = ptx::exp2_approx(s[32 * c + 2 * t] - m_use);
-            p1 = ptx::exp2_approx(s[32 * c + 2 * t + 1] - m_use);
-          }
-          rs0 += p0;
-          rs1 += p1;
+          float e0, e1;
+          if (scale_pos)
+            ptx::fma2(e0, e1, s[32 * c + 2 * t], s[32 * c + 2 * t + 1], scale_log2, scale_log2,
+                      -m_use, -m_use);
+          else
+            ptx::add2(e0, e1, s[32 * c + 2 * t], s[32 * c + 2 * t + 1], -m_use, -m_use);
+          const float p0 = ptx::exp2_approx(e0);
+          const float p1 = ptx::exp2_approx(e1);
+          ptx::add2(rs0, rs1, rs0, rs1, p0, p1);
           pr[t] = pack2<FP16>(p0, p1);
         }
         ptx::tmem_st_32x32b_x16(tS + c * 16, pr);
@@ -459,8 +475,13 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   const long long num_qblk = (p.N + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M);
   const dim3 grid(static_cast<unsigned>(num_qblk * p.B * p.H));
+  // Heads per dispatch group: K and V of a group within ~64 MiB of L2.
+  const long long kv_bytes_per_head = 4ll * p.N * p.d;
+  const long long bh = static_cast<long long>(p.B) * p.H;
+  const int heads_per_group =
+      static_cast<int>(std::max(1ll, std::min(bh, (64ll << 20) / kv_bytes_per_head)));
   kernel<<<grid, kThreads, smem, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.o, p.lse, p.H, p.N,
-                                           p.causal, p.scale_log2);
+                                           p.causal, p.scale_log2, heads_per_group);
   return cudaGetLastError();
 }
 
