@@ -235,6 +235,39 @@ def run_reference(args, w):
     return 0
 
 
+def time_standard_attention(q, k, v, w, steps, flush, stream):
+    """The standard three-step attention (S = QK^T, P = softmax(S), O = PV, with S and P
+    written to and read back from HBM), in PyTorch bf16/fp16 on the same device: the
+    comparison the pages make against the fused kernel. Times `steps` calls with the same L2
+    flush and per-step CUDA events; returns (mean ms, O in [B, N, H, d])."""
+    import torch
+    qh, kh, vh = (t.permute(0, 2, 1, 3).contiguous() for t in (q, k, v))   # [B, H, N, d]
+    mask = None
+    if w.causal:
+        mask = torch.ones(w.N, w.N, dtype=torch.bool, device=q.device).triu_(1)
+
+    def step():
+        s = torch.matmul(qh, kh.transpose(-1, -2)) * w.scale
+        if mask is not None:
+            s.masked_fill_(mask, float("-inf"))
+        p = torch.softmax(s, dim=-1)
+        return torch.matmul(p, vh)
+
+    for _ in range(2):
+        step()
+    times = []
+    out = None
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        out = step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.mean(times), out.permute(0, 2, 1, 3)
+
+
 def run_gpu(args, w):
     import torch
     import torch.distributed as dist
@@ -376,6 +409,22 @@ def run_gpu(args, w):
         }
         if peak_sus:
             line["roofline"]["frac_of_sustained"] = achieved / peak_sus
+        if args.vs_standard:
+            std_ms, o_std = time_standard_attention(q, k, v, w, min(args.steps, 20), flush,
+                                                    stream)
+            std = {"ms": std_ms, "tflops": flops / (std_ms * 1e-3) / 1e12,
+                   "fused_speedup": std_ms / kernel_ms,
+                   "what": "PyTorch matmul -> softmax -> matmul, S and P materialised in HBM, "
+                           "same dtype, same L2 flush and CUDA-event timing"}
+            if parity is not None:
+                import oracle
+                rows = sample_rows(w.B, w.H, w.N, 8, seed=w.seed + 5)
+                o_ref, _ = oracle.attention_rows(qb, kb, vb, rows, w.causal, w.scale,
+                                                 dtype=w.dtype)
+                idx = [torch.from_numpy(rows[:, c]).to(dev) for c in range(3)]
+                og = o_std[idx[0], idx[2], idx[1]].double().cpu().numpy()
+                std["parity_max_abs_o"] = float(np.abs(og - o_ref).max())
+            line["standard_attention"] = std
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = {k: v for k, v in
                                     cpu_baseline(w, qb, kb, vb, args.cpu_seconds).items()}
@@ -394,6 +443,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-check", action="store_true", help="skip the sampled parity check")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--vs-standard", action="store_true",
+                    help="also time standard (materialised S, P) attention in PyTorch")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-total-seconds", type=float, default=120.0)
     args = ap.parse_args()

@@ -67,6 +67,10 @@ WORKLOADS = {
     "n2000_d128_fp16_stress": Workload("n2000_d128_fp16_stress", 16, 32, 2000, 128, "fp16",
                                        False, 5000, q_scale=8.0, k_outlier_frac=0.01,
                                        k_outlier_scale=10.0),
+    # The shapes of the pages' fused-vs-standard comparison (d = 128 at N = 1K and 8K; batch and
+    # heads are not stated there, 2 x 16 is used).
+    "n1k_d128": Workload("n1k_d128", 2, 16, 1024, 128, "bf16", False, 6000),
+    "n8k_d128": Workload("n8k_d128", 2, 16, 8192, 128, "bf16", False, 7000),
 }
 
 
