@@ -75,7 +75,12 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attention.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i32, dbl, vp, vp]
     lib.oracle_attention_rows.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i32, dbl, vp,
                                           i64, vp, vp]
+    lib.oracle_attention_masked.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i32, i64, i64,
+                                            vp, dbl, vp, vp]
+    lib.oracle_attention_rows_masked.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i32, i64,
+                                                 i64, vp, dbl, vp, i64, vp, vp]
     for fn in (lib.oracle_decode, lib.oracle_attention, lib.oracle_attention_rows,
+               lib.oracle_attention_masked, lib.oracle_attention_rows_masked,
                lib.oracle_max_threads):
         fn.restype = i32
     lib.oracle_max_threads.argtypes = []
@@ -126,42 +131,57 @@ def decode(bits: np.ndarray, dtype: str, lib: ctypes.CDLL | None = None) -> np.n
     return out
 
 
+def _lengths(seqlens_k, B):
+    if seqlens_k is None:
+        return None, None
+    arr = np.ascontiguousarray(np.asarray(seqlens_k, dtype=np.int32).reshape(-1))
+    if arr.size != B:
+        raise ValueError("seqlens_k must have one entry per batch")
+    return arr, _ptr(arr)
+
+
 def attention(q, k, v, causal: bool, scale: float, dtype: str | None = None,
-              lib: ctypes.CDLL | None = None):
+              lib: ctypes.CDLL | None = None, window=(-1, -1), seqlens_k=None):
     """Plain fp64 attention over [B, N, H, d] inputs.
 
     ``dtype`` None: q, k, v are real arrays (converted to float64). ``dtype`` "bf16"/"fp16":
-    they are uint16 bit patterns of that type. Returns (o [B,N,H,d] float64,
-    lse [B,H,N] float64). ``scale`` is used exactly as given (pass float(np.float32(s)) to
-    match an fp32 scale).
+    they are uint16 bit patterns of that type. ``window`` = (left, right): key j is allowed
+    for query i only if j >= i - left (left >= 0) and j <= i + right (right >= 0); -1 means
+    no bound. ``seqlens_k``: optional per-batch key lengths (keys at or past the length do not
+    exist). Rows with no allowed key get O = 0 and LSE = -inf. Returns (o [B,N,H,d] float64,
+    lse [B,H,N] float64). ``scale`` is used exactly as given.
     """
     lib = lib or load()
     kind, (q, k, v) = _kind_and_arrays(q, k, v, dtype)
     if q.ndim != 4 or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must share one [B, N, H, d] shape")
     B, N, H, d = q.shape
+    lens, lens_ptr = _lengths(seqlens_k, B)
     o = np.empty((B, N, H, d), dtype=np.float64)
     lse = np.empty((B, H, N), dtype=np.float64)
-    rc = lib.oracle_attention(_ptr(q), _ptr(k), _ptr(v), kind, B, H, N, d, int(bool(causal)),
-                              float(scale), _ptr(o), _ptr(lse))
+    rc = lib.oracle_attention_masked(_ptr(q), _ptr(k), _ptr(v), kind, B, H, N, d,
+                                     int(bool(causal)), int(window[0]), int(window[1]),
+                                     lens_ptr, float(scale), _ptr(o), _ptr(lse))
     if rc:
-        raise RuntimeError("oracle_attention failed: %d" % rc)
+        raise RuntimeError("oracle_attention_masked failed: %d" % rc)
     return o, lse
 
 
 def attention_rows(q, k, v, rows, causal: bool, scale: float, dtype: str | None = None,
-                   lib: ctypes.CDLL | None = None):
+                   lib: ctypes.CDLL | None = None, window=(-1, -1), seqlens_k=None):
     """Selected output rows of the same attention. ``rows`` is an int array of (b, h, i)
     triples, shape [R, 3]. Returns (o_rows [R, d], lse_rows [R])."""
     lib = lib or load()
     kind, (q, k, v) = _kind_and_arrays(q, k, v, dtype)
     B, N, H, d = q.shape
+    lens, lens_ptr = _lengths(seqlens_k, B)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
     o = np.empty((rows.shape[0], d), dtype=np.float64)
     lse = np.empty((rows.shape[0],), dtype=np.float64)
-    rc = lib.oracle_attention_rows(_ptr(q), _ptr(k), _ptr(v), kind, B, H, N, d,
-                                   int(bool(causal)), float(scale), _ptr(rows), rows.shape[0],
-                                   _ptr(o), _ptr(lse))
+    rc = lib.oracle_attention_rows_masked(_ptr(q), _ptr(k), _ptr(v), kind, B, H, N, d,
+                                          int(bool(causal)), int(window[0]), int(window[1]),
+                                          lens_ptr, float(scale), _ptr(rows), rows.shape[0],
+                                          _ptr(o), _ptr(lse))
     if rc:
-        raise RuntimeError("oracle_attention_rows failed: %d" % rc)
+        raise RuntimeError("oracle_attention_rows_masked failed: %d" % rc)
     return o, lse

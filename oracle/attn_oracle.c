@@ -18,10 +18,17 @@
  *   "FlashAttention V2 核心原理与架构设计" §2.3: the kernel also keeps the per-row softmax
  *       denominator l and row maximum m; the oracle reports them as one log-sum-exp,
  *       LSE_i = m_i + ln(l_i), in units of scaled scores.
+ *   "FlashAttention 优化原理与实现要点解析" §8 names the mask kinds an implementation may
+ *       support: causal,
+ *       padding and sliding-window masks. The oracle takes all three as one rule per query:
+ *       key j is allowed for query i of batch b when j < len_b (padding: keys at or past the
+ *       batch's key length do not exist; len_b = N without a length array), j <= i (causal),
+ *       j >= i - window_left (window_left >= 0) and j <= i + window_right (window_right >= 0).
+ *       The allowed keys always form one interval [lo, hi). A row with no allowed key has
+ *       O = 0 and LSE = -inf (the sum l is 0).
  *
  * Layouts: q, k, v and o are [B, N, H, d] row-major (element (b, n, h, c) at
- * ((b*N + n)*H + h)*d + c); lse is [B, H, N]. Keys at positions >= N do not exist. With
- * `causal`, key j is allowed for query i only when j <= i.
+ * ((b*N + n)*H + h)*d + c); lse is [B, H, N]; the optional key lengths are int32 [B].
  *
  * There is no blocking, fusion or reordering here: one (b, h, i) row at a time, the three
  * passes in order. Rows are independent, so OpenMP spreads rows over host cores.
@@ -74,16 +81,31 @@ int oracle_decode(const uint16_t* bits, int64_t n, int kind, double* out) {
     return 0;
 }
 
-/* One output row: query i of head (b, h). `s` is scratch of at least N doubles. */
+/* The keys query i may attend to: [lo, hi). `len_b` is the batch's key length. */
+static void key_range(int64_t i, int causal, int64_t wl, int64_t wr, int64_t len_b,
+                      int64_t* lo, int64_t* hi) {
+    int64_t a = 0, z = len_b;
+    if (causal && i + 1 < z) z = i + 1;
+    if (wl >= 0 && i - wl > a) a = i - wl;
+    if (wr >= 0 && i + wr + 1 < z) z = i + wr + 1;
+    *lo = a;
+    *hi = z;
+}
+
+/* One output row: query i of head (b, h) over keys [lo, hi). `s` is scratch of >= N doubles. */
 static void attention_row(const void* q, const void* k, const void* v, int kind,
-                          int64_t N, int64_t H, int64_t d, int causal, double scale,
+                          int64_t N, int64_t H, int64_t d, int64_t lo, int64_t hi, double scale,
                           int64_t b, int64_t h, int64_t i, double* s, double* o_row,
                           double* lse_out) {
     const int64_t q_off = ((b * N + i) * H + h) * d;
-    const int64_t n_keys = causal ? i + 1 : N;   /* keys j in [0, n_keys) are allowed */
+    if (lo >= hi) {             /* no key allowed: O = 0, LSE = -inf */
+        for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+        *lse_out = -INFINITY;
+        return;
+    }
 
     /* Step 1: S[i, j] = scale * <q_i, k_j>. */
-    for (int64_t j = 0; j < n_keys; ++j) {
+    for (int64_t j = lo; j < hi; ++j) {
         const int64_t k_off = ((b * N + j) * H + h) * d;
         double dot = 0.0;
         for (int64_t c = 0; c < d; ++c) dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);
@@ -92,24 +114,30 @@ static void attention_row(const void* q, const void* k, const void* v, int kind,
 
     /* Softmax pass 1: the row maximum. */
     double m = -INFINITY;
-    for (int64_t j = 0; j < n_keys; ++j)
+    for (int64_t j = lo; j < hi; ++j)
         if (s[j] > m) m = s[j];
 
     /* Softmax pass 2: the sum of exponentials relative to the maximum. */
     double l = 0.0;
-    for (int64_t j = 0; j < n_keys; ++j) l += exp(s[j] - m);
+    for (int64_t j = lo; j < hi; ++j) l += exp(s[j] - m);
 
     /* Softmax pass 3: normalise, turning S[i, :] into P[i, :] in place. */
-    for (int64_t j = 0; j < n_keys; ++j) s[j] = exp(s[j] - m) / l;
+    for (int64_t j = lo; j < hi; ++j) s[j] = exp(s[j] - m) / l;
 
     /* Step 3: O[i, :] = P[i, :] V. */
     for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
-    for (int64_t j = 0; j < n_keys; ++j) {
+    for (int64_t j = lo; j < hi; ++j) {
         const int64_t v_off = ((b * N + j) * H + h) * d;
         for (int64_t c = 0; c < d; ++c) o_row[c] += s[j] * elem(v, kind, v_off + c);
     }
 
     *lse_out = m + log(l);
+}
+
+static int64_t batch_key_length(const int32_t* seqlens_k, int64_t b, int64_t N) {
+    if (!seqlens_k) return N;
+    int64_t len = seqlens_k[b];
+    return len < 0 ? 0 : (len > N ? N : len);
 }
 
 static int check_args(const void* q, const void* k, const void* v, int kind, int64_t B,
@@ -120,10 +148,11 @@ static int check_args(const void* q, const void* k, const void* v, int kind, int
     return 0;
 }
 
-/* Full attention: o [B, N, H, d], lse [B, H, N]. */
-int oracle_attention(const void* q, const void* k, const void* v, int kind, int64_t B,
-                     int64_t H, int64_t N, int64_t d, int causal, double scale, double* o,
-                     double* lse) {
+/* Full attention with the general mask: o [B, N, H, d], lse [B, H, N]. */
+int oracle_attention_masked(const void* q, const void* k, const void* v, int kind, int64_t B,
+                            int64_t H, int64_t N, int64_t d, int causal, int64_t window_left,
+                            int64_t window_right, const int32_t* seqlens_k, double scale,
+                            double* o, double* lse) {
     int rc = check_args(q, k, v, kind, B, H, N, d);
     if (rc) return rc;
     if (!o || !lse) return -1;
@@ -140,7 +169,10 @@ int oracle_attention(const void* q, const void* k, const void* v, int kind, int6
             for (int64_t r = 0; r < rows; ++r) {
                 /* r enumerates (b, h, i) with i fastest */
                 const int64_t i = r % N, h = (r / N) % H, b = r / (N * H);
-                attention_row(q, k, v, kind, N, H, d, causal, scale, b, h, i, s,
+                int64_t lo, hi;
+                key_range(i, causal, window_left, window_right,
+                          batch_key_length(seqlens_k, b, N), &lo, &hi);
+                attention_row(q, k, v, kind, N, H, d, lo, hi, scale, b, h, i, s,
                               o + ((b * N + i) * H + h) * d, lse + (b * H + h) * N + i);
             }
             free(s);
@@ -149,11 +181,18 @@ int oracle_attention(const void* q, const void* k, const void* v, int kind, int6
     return failed ? -4 : 0;
 }
 
+int oracle_attention(const void* q, const void* k, const void* v, int kind, int64_t B,
+                     int64_t H, int64_t N, int64_t d, int causal, double scale, double* o,
+                     double* lse) {
+    return oracle_attention_masked(q, k, v, kind, B, H, N, d, causal, -1, -1, 0, scale, o, lse);
+}
+
 /* Selected rows: rows[3t..3t+2] = (b, h, i); o_rows [nrows, d], lse_rows [nrows]. */
-int oracle_attention_rows(const void* q, const void* k, const void* v, int kind, int64_t B,
-                          int64_t H, int64_t N, int64_t d, int causal, double scale,
-                          const int64_t* rows, int64_t nrows, double* o_rows,
-                          double* lse_rows) {
+int oracle_attention_rows_masked(const void* q, const void* k, const void* v, int kind,
+                                 int64_t B, int64_t H, int64_t N, int64_t d, int causal,
+                                 int64_t window_left, int64_t window_right,
+                                 const int32_t* seqlens_k, double scale, const int64_t* rows,
+                                 int64_t nrows, double* o_rows, double* lse_rows) {
     int rc = check_args(q, k, v, kind, B, H, N, d);
     if (rc) return rc;
     if (!rows || !o_rows || !lse_rows || nrows < 0) return -1;
@@ -170,14 +209,26 @@ int oracle_attention_rows(const void* q, const void* k, const void* v, int kind,
             failed = 1;
         } else {
 #pragma omp for schedule(dynamic, 1)
-            for (int64_t t = 0; t < nrows; ++t)
-                attention_row(q, k, v, kind, N, H, d, causal, scale, rows[3 * t],
-                              rows[3 * t + 1], rows[3 * t + 2], s, o_rows + t * d,
-                              lse_rows + t);
+            for (int64_t t = 0; t < nrows; ++t) {
+                const int64_t b = rows[3 * t], h = rows[3 * t + 1], i = rows[3 * t + 2];
+                int64_t lo, hi;
+                key_range(i, causal, window_left, window_right,
+                          batch_key_length(seqlens_k, b, N), &lo, &hi);
+                attention_row(q, k, v, kind, N, H, d, lo, hi, scale, b, h, i, s,
+                              o_rows + t * d, lse_rows + t);
+            }
             free(s);
         }
     }
     return failed ? -4 : 0;
+}
+
+int oracle_attention_rows(const void* q, const void* k, const void* v, int kind, int64_t B,
+                          int64_t H, int64_t N, int64_t d, int causal, double scale,
+                          const int64_t* rows, int64_t nrows, double* o_rows,
+                          double* lse_rows) {
+    return oracle_attention_rows_masked(q, k, v, kind, B, H, N, d, causal, -1, -1, 0, scale,
+                                        rows, nrows, o_rows, lse_rows);
 }
 
 int oracle_max_threads(void) {

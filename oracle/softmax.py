@@ -19,7 +19,8 @@ tiled algorithm reaches the plain definition that ``attn_oracle.c`` computes:
   e^{m_old - m} and add P_block V_block (P_block taken relative to the updated m), and after
   the last K/V block divide O by l (§6: numerator and denominator kept apart until the end).
   Causal (§7): a query attends to keys at positions <= its own; K/V blocks that lie
-  entirely above the diagonal are skipped.
+  entirely above the diagonal are skipped. §8's padding and sliding-window masks take the
+  same form: a per-row key interval, and blocks with no allowed key are skipped.
 """
 from __future__ import annotations
 
@@ -73,15 +74,22 @@ def online_softmax(x, block_sizes) -> tuple[np.ndarray, float, float]:
     return np.exp(x - m) / l, m, l
 
 
-def blockwise_attention(q, k, v, Br: int, Bc: int, causal: bool, scale: float):
+def blockwise_attention(q, k, v, Br: int, Bc: int, causal: bool, scale: float,
+                        window=(-1, -1), kv_len=None):
     """Tiled attention with online softmax, fp64, for one head.
 
-    q, k, v: [N, d] float arrays. Returns (O [N, d], LSE [N]) with LSE = m + ln l.
+    q, k, v: [N, d] float arrays. ``window`` = (left, right) bounds the keys a query sees
+    (j >= i - left, j <= i + right; -1 = no bound); ``kv_len`` (default N): keys at or past it
+    do not exist. K/V blocks with no allowed key for any row of the Q block are skipped.
+    Returns (O [N, d], LSE [N]) with LSE = m + ln l; rows with no allowed key get O = 0 and
+    LSE = -inf.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     N, d = q.shape
+    kv_len = N if kv_len is None else kv_len
+    left, right = window
     O = np.zeros((N, d))
     LSE = np.zeros(N)
     for i0 in range(0, N, Br):                        # outer loop: Q blocks
@@ -92,11 +100,16 @@ def blockwise_attention(q, k, v, Br: int, Bc: int, causal: bool, scale: float):
         Oi = np.zeros((rows.size, d))
         for j0 in range(0, N, Bc):                    # inner loop: K/V blocks
             cols = np.arange(j0, min(j0 + Bc, N))
-            if causal and cols[0] > rows[-1]:
-                break                                 # block entirely above the diagonal
-            S = scale * (Qi @ k[cols].T)              # local scores
+            allowed = cols[None, :] < kv_len
             if causal:
-                S = np.where(cols[None, :] <= rows[:, None], S, -math.inf)
+                allowed = allowed & (cols[None, :] <= rows[:, None])
+            if left >= 0:
+                allowed = allowed & (cols[None, :] >= rows[:, None] - left)
+            if right >= 0:
+                allowed = allowed & (cols[None, :] <= rows[:, None] + right)
+            if not allowed.any():
+                continue                              # block fully masked: skipped
+            S = np.where(allowed, scale * (Qi @ k[cols].T), -math.inf)   # local scores
             m_blk = S.max(axis=1)                     # local maximum
             m_new = np.maximum(m, m_blk)
             # rows whose keys so far are all masked keep m = -inf; shift by 0 instead
@@ -106,6 +119,7 @@ def blockwise_attention(q, k, v, Br: int, Bc: int, causal: bool, scale: float):
             l = l * alpha + P.sum(axis=1)
             Oi = Oi * alpha[:, None] + P @ v[cols]
             m = m_new
-        O[rows] = Oi / l[:, None]                     # normalise once, at the end
-        LSE[rows] = m + np.log(l)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            O[rows] = np.where(l[:, None] > 0, Oi / np.where(l > 0, l, 1.0)[:, None], 0.0)
+            LSE[rows] = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -math.inf)
     return O, LSE

@@ -171,8 +171,10 @@ def pin_kv_permutation(lib):
     assert np.abs(l1 - l0).max() < 1e-13
 
 
-def _brute_force_mp(q, k, v, causal, scale):
-    """sum_j e^{s_j} v_j / sum_j e^{s_j} in 60-digit arithmetic, no max shift."""
+def _brute_force_mp(q, k, v, causal, scale, allowed=None):
+    """sum_j e^{s_j} v_j / sum_j e^{s_j} in 60-digit arithmetic, no max shift. ``allowed``
+    (b, i, j) -> bool restricts the keys (default: all, or j <= i when causal); a row with no
+    allowed key gives O = 0, LSE = -inf."""
     import mpmath
     mp = mpmath.mp.clone()
     mp.dps = 60
@@ -182,7 +184,13 @@ def _brute_force_mp(q, k, v, causal, scale):
     for b in range(B):
         for h in range(H):
             for i in range(N):
-                js = range(i + 1) if causal else range(N)
+                if allowed is None:
+                    js = list(range(i + 1) if causal else range(N))
+                else:
+                    js = [j for j in range(N) if allowed(b, i, j)]
+                if not js:
+                    lse[b, h, i] = -math.inf
+                    continue
                 ws = []
                 for j in js:
                     s = mp.mpf(0)
@@ -271,9 +279,102 @@ def pin_dtype_inputs(lib):
             assert np.array_equal(o_r[t], o_bits[b, i, h]) and l_r[t] == l_bits[b, h, i]
 
 
+def pin_padding_is_truncation(lib):
+    """Per-batch key lengths (padding mask) give, for every query, exactly the attention over
+    the first len_b keys and values; a zero length gives O = 0, LSE = -inf."""
+    B, N, H, d = 3, 21, 2, 8
+    rng = _rng(22)
+    q, k, v = (rng.standard_normal((B, N, H, d)) for _ in range(3))
+    lens = [21, 9, 0]
+    for causal in (False, True):
+        o, lse = oracle.attention(q, k, v, causal, 0.4, lib=lib, seqlens_k=lens)
+        for b, L in enumerate(lens):
+            if L == 0:
+                assert (o[b] == 0).all() and (lse[b] == -np.inf).all()
+                continue
+            # queries keep all N positions; keys and values are cut to the first L rows
+            for i in range(N):
+                ob, lb = _brute_force_rows(q[b], k[b, :L], v[b, :L], causal, 0.4, i)
+                assert np.abs(o[b, i] - ob).max() < 1e-12
+                assert np.abs(lse[b, :, i] - lb).max() < 1e-12
+
+
+def _brute_force_rows(qb, kb, vb, causal, scale, i):
+    """Row i of attention for one batch (all heads) in float64, keys [0, len(kb)), direct
+    softmax via numpy (no shared code with the oracle)."""
+    L, H = kb.shape[0], qb.shape[1]
+    o = np.zeros((H, qb.shape[2]))
+    lse = np.full(H, -np.inf)
+    js = [j for j in range(L) if (not causal or j <= i)]
+    if not js:
+        return o, lse
+    for h in range(H):
+        sc = np.array([scale * float(qb[i, h] @ kb[j, h]) for j in js])
+        mx = sc.max()
+        w = np.exp(sc - mx)
+        o[h] = (w[:, None] * vb[js, h]).sum(0) / w.sum()
+        lse[h] = mx + math.log(w.sum())
+    return o, lse
+
+
+def pin_sliding_window_brute_force(lib):
+    """Sliding windows (left / right bounds, with and without causal) equal the 60-digit
+    brute force over the explicitly listed allowed keys, including rows left empty."""
+    rng = _rng(23)
+    B, N, H, d = 1, 14, 2, 6
+    q, k, v = (rng.standard_normal((B, N, H, d)) for _ in range(3))
+    lens = [11]
+    for causal, (left, right) in [(True, (3, -1)), (False, (2, 4)), (False, (-1, 1)),
+                                  (True, (0, -1)), (False, (5, 0)), (True, (2, 1))]:
+        def allowed(b, i, j, causal=causal, left=left, right=right):
+            return (j < lens[b] and (not causal or j <= i) and (left < 0 or j >= i - left)
+                    and (right < 0 or j <= i + right))
+        o, lse = oracle.attention(q, k, v, causal, 0.5, lib=lib, window=(left, right),
+                                  seqlens_k=lens)
+        ob, lb = _brute_force_mp(q, k, v, causal, 0.5, allowed=allowed)
+        assert np.abs(o - ob).max() < 1e-12
+        fin = np.isfinite(lb)
+        assert np.array_equal(fin, np.isfinite(lse))
+        assert np.abs(lse[fin] - lb[fin]).max() < 1e-12
+
+
+def pin_window_special_cases(lib):
+    """Causal with window_left = 0: each query sees only itself (O = V_i, LSE = scale <q_i,
+    k_i>); windows at least N wide change nothing."""
+    rng = _rng(24)
+    B, N, H, d = 2, 19, 2, 8
+    q, k, v = (rng.standard_normal((B, N, H, d)) for _ in range(3))
+    o, lse = oracle.attention(q, k, v, True, 0.3, lib=lib, window=(0, -1))
+    assert np.abs(o - v).max() < 1e-15
+    assert np.abs(lse - 0.3 * np.einsum("bnhc,bnhc->bhn", q, k)).max() < 1e-13
+    for causal in (False, True):
+        o0, l0 = oracle.attention(q, k, v, causal, 0.3, lib=lib)
+        o1, l1 = oracle.attention(q, k, v, causal, 0.3, lib=lib, window=(N, N))
+        assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
+def pin_tiled_algorithm_masks(lib):
+    """The tiled algorithm with padding / window masks and block skipping reaches the plain
+    definition, for ragged block shapes."""
+    rng = _rng(25)
+    N, d = 41, 8
+    q, k, v = (rng.standard_normal((1, N, 1, d)) for _ in range(3))
+    for causal, window, L in [(True, (7, -1), 41), (False, (5, 5), 30), (True, (-1, -1), 17),
+                              (False, (-1, 0), 41), (True, (3, -1), 2)]:
+        o, lse = oracle.attention(q, k, v, causal, 0.4, lib=lib, window=window, seqlens_k=[L])
+        for Br, Bc in [(8, 8), (16, 7), (64, 16)]:
+            ot, lt = oracle.blockwise_attention(q[0, :, 0], k[0, :, 0], v[0, :, 0], Br, Bc,
+                                                causal, 0.4, window=window, kv_len=L)
+            assert np.abs(ot - o[0, :, 0]).max() < 1e-12
+            fin = np.isfinite(lse[0, 0])
+            assert np.array_equal(fin, np.isfinite(lt))
+            assert np.abs(lt[fin] - lse[0, 0][fin]).max() < 1e-12
+
+
 ALL_PINS = [
     pin_decode_fp16, pin_decode_bf16, pin_probability_rows, pin_zero_queries,
     pin_constant_values, pin_causal_first_row, pin_single_token, pin_two_key_closed_form,
     pin_key_shift, pin_kv_permutation, pin_brute_force_small, pin_brute_force_large_logits,
-    pin_tiled_algorithm, pin_torch_math_sdpa, pin_dtype_inputs,
+    pin_tiled_algorithm, pin_torch_math_sdpa, pin_dtype_inputs, pin_padding_is_truncation,
+    pin_sliding_window_brute_force, pin_window_special_cases, pin_tiled_algorithm_masks,
 ]

@@ -16,8 +16,15 @@ MUTANTS = [
      "dot += elem(k, kind, q_off + c) * elem(q, kind, k_off + c);"),
     ("query_row_for_value", "const int64_t v_off = ((b * N + j) * H + h) * d;",
      "const int64_t v_off = ((b * N + i) * H + h) * d;"),
-    ("causal_excludes_diagonal", "causal ? i + 1 : N;", "causal ? i : N;"),
-    ("causal_off_by_one_extra", "causal ? i + 1 : N;", "causal ? (i + 2 < N ? i + 2 : N) : N;"),
+    ("causal_excludes_diagonal", "if (causal && i + 1 < z) z = i + 1;",
+     "if (causal && i < z) z = i;"),
+    ("causal_off_by_one_extra", "if (causal && i + 1 < z) z = i + 1;",
+     "if (causal && i + 2 < z) z = i + 2;"),
+    ("window_left_off_by_one", "if (wl >= 0 && i - wl > a) a = i - wl;",
+     "if (wl >= 0 && i - wl + 1 > a) a = i - wl + 1;"),
+    ("window_right_ignored", "if (wr >= 0 && i + wr + 1 < z) z = i + wr + 1;", ""),
+    ("padding_ignored", "if (!seqlens_k) return N;", "return N;"),
+    ("empty_row_lse_zero", "*lse_out = -INFINITY;", "*lse_out = 0.0;"),
     ("scale_dropped", "s[j] = scale * dot;", "s[j] = dot;"),
     ("scale_squared", "s[j] = scale * dot;", "s[j] = scale * scale * dot;"),
     ("lse_without_max", "*lse_out = m + log(l);", "*lse_out = log(l);"),
@@ -27,8 +34,8 @@ MUTANTS = [
      "const int64_t k_off = ((b * N + j) * H + 0) * d;"),
     ("batch_index_ignored", "const int64_t q_off = ((b * N + i) * H + h) * d;",
      "const int64_t q_off = ((0 * N + i) * H + h) * d;"),
-    ("max_over_prefix_only", "for (int64_t j = 0; j < n_keys; ++j)\n        if (s[j] > m)",
-     "for (int64_t j = 0; j < n_keys / 2; ++j)\n        if (s[j] > m)"),
+    ("max_over_prefix_only", "for (int64_t j = lo; j < hi; ++j)\n        if (s[j] > m)",
+     "for (int64_t j = lo; j < lo + (hi - lo) / 2; ++j)\n        if (s[j] > m)"),
     ("fp16_bias_wrong", "ldexp((double)(1024 + mant), expo - 25)",
      "ldexp((double)(1024 + mant), expo - 24)"),
     ("fp16_subnormal_wrong", "ldexp((double)mant, -24)", "ldexp((double)mant, -25)"),
