@@ -50,8 +50,8 @@ enum fa_status {
     FA_ERR_NULL = -1,     /* a required pointer is NULL */
     FA_ERR_SHAPE = -2,    /* B, H or N < 1; d not 64 or 128; or B*N*H*d does not fit int64 */
     FA_ERR_DTYPE = -3,    /* dtype is not an fa_dtype */
-    FA_ERR_ALIGN = -4,    /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
-    FA_ERR_ALIAS = -5,    /* o or lse overlaps q, k or v, or o overlaps lse */
+    FA_ERR_ALIGN = -4,    /* q, k, v or o not 16-byte aligned; lse or seqlens_k not 4-byte */
+    FA_ERR_ALIAS = -5,    /* o or lse overlaps q, k, v or seqlens_k, or o overlaps lse */
     FA_ERR_ARCH = -6,     /* the current device is not compute capability 10.3 (sm_103) */
     FA_ERR_LAUNCH = -7,   /* the kernel launch failed (the CUDA error is not cleared) */
     FA_ERR_TIMEOUT = -8,  /* a kernel wait ran past its limit; outputs are undefined */
@@ -80,6 +80,26 @@ enum fa_status {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
            int N, int d, int causal, float scale, int dtype, fa_stream_t stream);
+
+/*
+ * fa_fwd_masked -- fa_fwd with the padding and sliding-window masks named next to the causal
+ * mask in "FlashAttention 优化原理与实现要点解析" §8. Key j is visible to query i of batch b
+ * only when all of these hold:
+ *   j < len_b                  padding: len_b = seqlens_k[b] clamped to [0, N], or N when
+ *                              seqlens_k is NULL (keys at or past len_b do not exist)
+ *   j <= i                     when causal is nonzero
+ *   j >= i - window_left       when window_left >= 0 (negative: no bound)
+ *   j <= i + window_right      when window_right >= 0 (negative: no bound)
+ * A query with no visible key gets O = 0 and LSE = -inf. K/V tiles with no visible key for any
+ * query of a Q tile are never loaded or multiplied.
+ *
+ *   seqlens_k  device int32 [B], 4-byte aligned, read only, or NULL; it must not overlap o or
+ *              lse (FA_ERR_ALIAS). Its values are read by the kernel, not checked on the host.
+ *   everything else as in fa_fwd; fa_fwd(...) equals fa_fwd_masked(..., -1, -1, NULL, ...).
+ */
+int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int H, int N, int d, int causal, int window_left, int window_right,
+                  const int* seqlens_k, float scale, int dtype, fa_stream_t stream);
 
 /* Static English text for a status code (never NULL). */
 const char* fa_error_string(int code);

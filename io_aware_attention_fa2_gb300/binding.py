@@ -47,6 +47,9 @@ def load_library() -> ctypes.CDLL:
             vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
             lib.fa_fwd.restype = i32
+            lib.fa_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                          vp, f32, i32, vp]
+            lib.fa_fwd_masked.restype = i32
             lib.fa_error_string.argtypes = [i32]
             lib.fa_error_string.restype = ctypes.c_char_p
             lib.fa_get_device_error.argtypes = [vp]
@@ -92,11 +95,15 @@ def _dtype_code(t) -> int:
     raise TypeError("q, k, v must be bfloat16 or float16, got %s" % t.dtype)
 
 
-def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None, window=(-1, -1),
+           seqlens_k=None) -> None:
     """Enqueue the attention forward on ``stream`` (default: torch's current stream).
 
     q, k, v, o: CUDA tensors [B, N, H, d] of one dtype (bf16/fp16), contiguous.
     lse: CUDA float32 tensor [B, H, N], contiguous.
+    window: (left, right) sliding-window bounds (negative = none); seqlens_k: optional CUDA
+    int32 tensor [B] of per-batch key lengths (padding mask). Either one selects
+    ``fa_fwd_masked``; otherwise ``fa_fwd`` is called.
     """
     import torch
     if q.dim() != 4:
@@ -110,11 +117,25 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("%s must be a contiguous CUDA tensor" % name)
-    rc = load_library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                               lse.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
-                               _dtype_code(q), _stream_handle(stream))
+    lib = load_library()
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+            int(bool(causal)))
+    left, right = (int(w) for w in window)
+    if seqlens_k is None and left < 0 and right < 0:
+        rc = lib.fa_fwd(*args, float(scale), _dtype_code(q), _stream_handle(stream))
+        where = "fa_fwd"
+    else:
+        lens_ptr = None
+        if seqlens_k is not None:
+            if (not seqlens_k.is_cuda or seqlens_k.dtype != torch.int32
+                    or seqlens_k.shape != (B,) or not seqlens_k.is_contiguous()):
+                raise ValueError("seqlens_k must be a contiguous CUDA int32 tensor [B]")
+            lens_ptr = seqlens_k.data_ptr()
+        rc = lib.fa_fwd_masked(*args, left, right, lens_ptr, float(scale), _dtype_code(q),
+                               _stream_handle(stream))
+        where = "fa_fwd_masked"
     if rc != FA_OK:
-        raise FaError(rc, "fa_fwd")
+        raise FaError(rc, where)
 
 
 def device_error(stream=None) -> int:
@@ -123,13 +144,14 @@ def device_error(stream=None) -> int:
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
-                      lse=None, stream=None, device=None):
+                      lse=None, stream=None, device=None, window=(-1, -1), seqlens_k=None):
     """O, LSE = attention(q, k, v). The call a user makes.
 
     Device tensors are used in place. Host tensors (ideally pinned) are copied to ``device``
     (default cuda:0) on ``stream``, the kernel runs there, and O and LSE are copied back into
     host tensors, so the result is ready when the call returns. ``scale`` defaults to
-    1/sqrt(d) rounded to fp32.
+    1/sqrt(d) rounded to fp32. ``window`` and ``seqlens_k`` (int32 [B], host or device) select
+    the padding and sliding-window masks (see ``fa_fwd``).
     """
     import math
 
@@ -141,7 +163,8 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         o = out if out is not None else torch.empty_like(q)
         ls = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32,
                                                      device=q.device)
-        fa_fwd(q, k, v, o, ls, causal, scale, stream)
+        lens = None if seqlens_k is None else seqlens_k.to(q.device, torch.int32)
+        fa_fwd(q, k, v, o, ls, causal, scale, stream, window, lens)
         return o, ls
     dev = torch.device(device or "cuda:0")
     st = stream if stream is not None else torch.cuda.current_stream(dev)
@@ -149,7 +172,8 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
         od = torch.empty_like(qd)
         ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        fa_fwd(qd, kd, vd, od, ld, causal, scale, st)
+        lens = None if seqlens_k is None else seqlens_k.to(dev, torch.int32, non_blocking=True)
+        fa_fwd(qd, kd, vd, od, ld, causal, scale, st, window, lens)
         o_host = out if out is not None else torch.empty(q.shape, dtype=q.dtype,
                                                          pin_memory=q.is_pinned())
         l_host = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32,

@@ -86,8 +86,9 @@ const char* fa_error_string(int code) {
     case FA_ERR_NULL: return "a required pointer is NULL";
     case FA_ERR_SHAPE: return "unsupported shape (B, H, N >= 1; d in {64, 128}; size overflow)";
     case FA_ERR_DTYPE: return "dtype is not FA_BF16 or FA_FP16";
-    case FA_ERR_ALIGN: return "misaligned pointer (q, k, v, o: 16 bytes; lse: 4 bytes)";
-    case FA_ERR_ALIAS: return "an output overlaps an input or the other output";
+    case FA_ERR_ALIGN:
+      return "misaligned pointer (q, k, v, o: 16 bytes; lse, seqlens_k: 4 bytes)";
+    case FA_ERR_ALIAS: return "an output overlaps an input, seqlens_k or the other output";
     case FA_ERR_ARCH: return "the current device is not sm_103 (GB300)";
     case FA_ERR_LAUNCH: return "kernel launch failed";
     case FA_ERR_TIMEOUT: return "a kernel wait ran past its limit";
@@ -99,6 +100,13 @@ const char* fa_error_string(int code) {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
            int N, int d, int causal, float scale, int dtype, fa_stream_t stream) {
+  return fa_fwd_masked(q, k, v, o, lse, B, H, N, d, causal, -1, -1, nullptr, scale, dtype,
+                       stream);
+}
+
+int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int H, int N, int d, int causal, int window_left, int window_right,
+                  const int* seqlens_k, float scale, int dtype, fa_stream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return FA_ERR_SHAPE;
   if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
@@ -114,6 +122,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   for (const void* p : {q, k, v, static_cast<const void*>(o)})
     if (reinterpret_cast<uintptr_t>(p) % 16) return FA_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(lse) % 4) return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(seqlens_k) % 4) return FA_ERR_ALIGN;
+  if (seqlens_k && (overlaps(seqlens_k, (uint64_t)B * 4, o, t_bytes) ||
+                    overlaps(seqlens_k, (uint64_t)B * 4, lse, lse_bytes)))
+    return FA_ERR_ALIAS;
   for (const void* in : {q, k, v})
     if (overlaps(o, t_bytes, in, t_bytes) || overlaps(lse, lse_bytes, in, t_bytes))
       return FA_ERR_ALIAS;
@@ -135,6 +147,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.N = N;
   p.d = d;
   p.causal = causal ? 1 : 0;
+  p.window_left = window_left < 0 ? -1 : window_left;
+  p.window_right = window_right < 0 ? -1 : window_right;
+  p.seqlens_k = seqlens_k;
   p.fp16 = fp16 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   if (fa::launch_fwd(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -109,11 +109,40 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// Number of K/V tiles Q tile `qt` (128 rows) visits: all of them, or, when causal, those at
-// or below the diagonal.
-__device__ __forceinline__ int kv_tiles_for(int qt, int num_kv_total, int causal) {
-  return causal ? min(qt + 1, num_kv_total) : num_kv_total;
-}
+// Which keys a query may attend to ("FlashAttention 优化原理与实现要点解析" §7 causal mask and
+// the padding and sliding-window masks §8 names): key j is allowed for query i when
+// j < len (the batch's key length), j <= i (causal), j >= i - left (left >= 0) and
+// j <= i + right (right >= 0). The allowed keys of one query form the interval [lo(i), hi(i)),
+// and lo, hi never decrease with i.
+struct KeyMask {
+  int len, causal, left, right;
+  __device__ __forceinline__ int lo(int i) const { return left >= 0 ? max(0, i - left) : 0; }
+  __device__ __forceinline__ int hi(int i) const {
+    int z = len;
+    if (causal) z = min(z, i + 1);
+    if (right >= 0) z = min(z, i + right + 1);
+    return z;
+  }
+  // K/V tiles [j0, j1) that hold an allowed key of some row of Q tile qt (rows < N only);
+  // j1 <= j0 when there is none.
+  __device__ __forceinline__ void tile_range(int qt, int N, int& j0, int& j1) const {
+    const int r0 = qt * BLOCK_M;
+    const int r_last = min(r0 + BLOCK_M, N) - 1;
+    const int a = lo(r0), z = r0 < N ? hi(r_last) : 0;
+    if (z <= a) {
+      j0 = 0;
+      j1 = 0;
+    } else {
+      j0 = a / BLOCK_N;
+      j1 = (z + BLOCK_N - 1) / BLOCK_N;
+    }
+  }
+  // True when K/V tile j needs no per-element mask for any row of Q tile qt.
+  __device__ __forceinline__ bool tile_full(int qt, int j) const {
+    const int r0 = qt * BLOCK_M, k0 = j * BLOCK_N;
+    return k0 >= lo(r0 + BLOCK_M - 1) && k0 + BLOCK_N <= hi(r0);
+  }
+};
 
 // ---------------------------------------------------------------------------------------------
 template <int D, bool FP16>
@@ -122,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
                   float* __restrict__ lse_ptr, int H, int N, int causal, float scale_log2,
-                  int heads_per_group) {
+                  int heads_per_group, int window_left, int window_right,
+                  const int* __restrict__ seqlens_k) {
   using L = SmemLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_base_slot;
@@ -151,9 +181,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = rem / g_size;
   const int qblk = causal ? num_qblk - 1 - r : r;
   const int b = bh / H, h = bh % H;
-  const int num_kv_total = (N + BLOCK_N - 1) / BLOCK_N;
-  const int n_a = kv_tiles_for(kQTiles * qblk, num_kv_total, causal);
-  const int n_b = kv_tiles_for(kQTiles * qblk + 1, num_kv_total, causal);   // n_b >= n_a
+  KeyMask mask;
+  mask.len = seqlens_k ? min(max(seqlens_k[b], 0), N) : N;
+  mask.causal = causal;
+  mask.left = window_left;
+  mask.right = window_right;
+  // K/V tile ranges of tile A and tile B ([x0, x1), empty when x1 <= x0; a0 <= b0 and
+  // a1 <= b1 when both are non-empty) and their union [u0, u1), which the producer streams.
+  int a0, a1, b0, b1;
+  mask.tile_range(kQTiles * qblk, N, a0, a1);
+  mask.tile_range(kQTiles * qblk + 1, N, b0, b1);
+  const bool a_any = a1 > a0, b_any = b1 > b0;
+  const int u0 = a_any ? a0 : b0;
+  const int u1 = b_any ? b1 : a1;
+  const bool any_work = a_any || b_any;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -184,7 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // K/V tiles u0, u0+1, ..., u1-1 go through the rings in order; load n of the sequence uses
+    // stage n % kStages.
+    if (lane == 0 && any_work) {
       ptx::prefetch_tensormap(&tm_q);
       ptx::prefetch_tensormap(&tm_k);
       ptx::prefetch_tensormap(&tm_v);
@@ -193,11 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < D / BOX_COLS; ++c)
           ptx::tma_load_4d(sQ + x * L::kTile + c * kBoxBytes, &tm_q, bar(BAR_Q_FULL),
                            c * BOX_COLS, h, (kQTiles * qblk + x) * BLOCK_M, b);
-      int issued = 0;
-      for (int j = 0; j < n_b; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        const int kv_row0 = j * BLOCK_N;
+      int k_issued = 0, v_issued = 0;
+      for (int n = 0; n < u1 - u0; ++n) {
+        const int s = n % kStages;
+        const uint32_t ph = (n / kStages) & 1;
+        const int kv_row0 = (u0 + n) * BLOCK_N;
         if (!ptx::wait_bounded(bar(BAR_K_EMPTY + s), ph ^ 1, abort_p, kWaitLimitNs)) {
           record_timeout(abort_p);
           break;
@@ -206,27 +249,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < D / BOX_COLS; ++c)
           ptx::tma_load_4d(sK + s * L::kTile + c * kBoxBytes, &tm_k, bar(BAR_K_FULL + s),
                            c * BOX_COLS, h, kv_row0, b);
+        k_issued = n + 1;
         if (!ptx::wait_bounded(bar(BAR_V_EMPTY + s), ph ^ 1, abort_p, kWaitLimitNs)) {
           record_timeout(abort_p);
-          issued = -(j + 1);   // K_j issued, V_j not
           break;
         }
         ptx::mbar_arrive_expect_tx(bar(BAR_V_FULL + s), L::kTile);
         for (int c = 0; c < D / BOX_COLS; ++c)
           ptx::tma_load_4d(sV + s * L::kTile + c * kBoxBytes, &tm_v, bar(BAR_V_FULL + s),
                            c * BOX_COLS, h, kv_row0, b);
-        issued = j + 1;
+        v_issued = n + 1;
       }
       // Leave no copy in flight: wait (bounded) for Q and for the last load into every stage.
       // On the normal path these phases completed long ago.
       ptx::wait_bounded(bar(BAR_Q_FULL), 0, abort_p, kWaitLimitNs);
-      const int k_issued = issued < 0 ? -issued : issued;
-      const int v_issued = issued < 0 ? -issued - 1 : issued;
-      for (int j = (k_issued > kStages ? k_issued - kStages : 0); j < k_issued; ++j)
-        ptx::wait_bounded(bar(BAR_K_FULL + j % kStages), (j / kStages) & 1, abort_p,
+      for (int n = (k_issued > kStages ? k_issued - kStages : 0); n < k_issued; ++n)
+        ptx::wait_bounded(bar(BAR_K_FULL + n % kStages), (n / kStages) & 1, abort_p,
                           kWaitLimitNs);
-      for (int j = (v_issued > kStages ? v_issued - kStages : 0); j < v_issued; ++j)
-        ptx::wait_bounded(bar(BAR_V_FULL + j % kStages), (j / kStages) & 1, abort_p,
+      for (int n = (v_issued > kStages ? v_issued - kStages : 0); n < v_issued; ++n)
+        ptx::wait_bounded(bar(BAR_V_FULL + n % kStages), (n / kStages) & 1, abort_p,
                           kWaitLimitNs);
     }
   } else if (warp == 1) {
@@ -237,11 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait = [&](int slot, uint32_t parity) {
         return ptx::wait_bounded(bar(slot), parity, abort_p, kWaitLimitNs);
       };
-      // S_x(j) = Q_x K_j^T into the S columns of tile x.
+      // S_x(j) = Q_x K_j^T into the S columns of tile x (K_j sits in stage (j - u0) % kStages).
       auto issue_s = [&](int x, int j) {
         ptx::tc_fence_after_sync();
         const uint32_t q_base = sQ + x * L::kTile;
-        const uint32_t k_base = sK + (j % kStages) * L::kTile;
+        const uint32_t k_base = sK + ((j - u0) % kStages) * L::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // 16 elements (32 bytes) of d per MMA: 4 steps inside one 128-byte swizzle span,
@@ -254,51 +295,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // O_x += P_x(j) V_j: A = P_x from TMEM (16 keys = 8 columns per MMA), B = V tile,
       // MN-major (d contiguous): 16 keys = 16 rows of 128 bytes per MMA, LBO = next 64-column box.
-      auto issue_pv = [&](int x, int j) {
+      // The first P V of a tile overwrites O instead of accumulating.
+      auto issue_pv = [&](int x, int j, bool first) {
         ptx::tc_fence_after_sync();
-        const uint32_t v_base = sV + (j % kStages) * L::kTile;
+        const uint32_t v_base = sV + ((j - u0) % kStages) * L::kTile;
 #pragma unroll
         for (int kk = 0; kk < BLOCK_N / 16; ++kk)
           ptx::mma_f16_ts(tmem + kTmemO + x * D, tmem + x * BLOCK_N + kk * 8,
                           ptx::smem_desc_sw128(v_base + kk * 16 * 128, kBoxBytes, 1024),
-                          idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                          idesc_pv, (!first || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar(BAR_O_DONE + x));
       };
 
-      bool ok = wait(BAR_Q_FULL, 0) && wait(BAR_K_FULL + 0, 0);
-      if (ok) {
-        issue_s(0, 0);
-        issue_s(1, 0);
-        ptx::mma_commit(bar(BAR_K_EMPTY + 0));
+      auto on_a = [&](int j) { return a0 <= j && j < a1; };
+      auto on_b = [&](int j) { return b0 <= j && j < b1; };
+      // K_j / V_j are load number j - u0 of the sequence.
+      auto wait_k = [&](int j) {
+        return wait(BAR_K_FULL + (j - u0) % kStages, ((j - u0) / kStages) & 1);
+      };
+      auto wait_v = [&](int j) {
+        return wait(BAR_V_FULL + (j - u0) % kStages, ((j - u0) / kStages) & 1);
+      };
+      bool ok = true;
+      if (any_work) {
+        ok = wait(BAR_Q_FULL, 0) && wait_k(u0);
+        if (ok) {
+          if (on_a(u0)) issue_s(0, u0);
+          if (on_b(u0)) issue_s(1, u0);
+          ptx::mma_commit(bar(BAR_K_EMPTY + 0));
+        }
       }
-      for (int j = 0; ok && j < n_b; ++j) {
-        const int s = j % kStages;
-        bool k_next_ready = false;
-        if (!wait(BAR_V_FULL + s, (j / kStages) & 1)) { ok = false; break; }
-        if (j < n_a) {
-          if (!wait(BAR_P_FULL + 0, j & 1)) { ok = false; break; }
-          issue_pv(0, j);
-          if (j + 1 < n_a) {
-            if (!wait(BAR_K_FULL + (j + 1) % kStages, ((j + 1) / kStages) & 1)) {
-              ok = false;
-              break;
-            }
-            issue_s(0, j + 1);
-            k_next_ready = true;
-          }
+      // Per K/V tile j: P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1). The softmax of one tile
+      // runs while the tensor pipe works on the other.
+      for (int j = u0; ok && any_work && j < u1; ++j) {
+        const int s = (j - u0) % kStages;
+        const bool next = j + 1 < u1;
+        if (!wait_v(j)) { ok = false; break; }
+        if (next && !wait_k(j + 1)) { ok = false; break; }
+        if (on_a(j)) {
+          if (!wait(BAR_P_FULL + 0, (j - a0) & 1)) { ok = false; break; }
+          issue_pv(0, j, j == a0);
         }
-        if (!wait(BAR_P_FULL + 1, j & 1)) { ok = false; break; }
-        issue_pv(1, j);
+        if (on_a(j + 1)) issue_s(0, j + 1);
+        if (on_b(j)) {
+          if (!wait(BAR_P_FULL + 1, (j - b0) & 1)) { ok = false; break; }
+          issue_pv(1, j, j == b0);
+        }
         ptx::mma_commit(bar(BAR_V_EMPTY + s));
-        if (j + 1 < n_b) {
-          if (!k_next_ready &&
-              !wait(BAR_K_FULL + (j + 1) % kStages, ((j + 1) / kStages) & 1)) {
-            ok = false;
-            break;
-          }
-          issue_s(1, j + 1);
-          ptx::mma_commit(bar(BAR_K_EMPTY + (j + 1) % kStages));
-        }
+        if (on_b(j + 1)) issue_s(1, j + 1);
+        if (next) ptx::mma_commit(bar(BAR_K_EMPTY + (j + 1 - u0) % kStages));
       }
       if (!ok) record_timeout(abort_p);
       // Every MMA this thread issued has completed before TMEM can be released.
@@ -313,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;                // query row within the tile
     const int qt = kQTiles * qblk + x;                  // global Q tile index
     const int q_idx = qt * BLOCK_M + row;               // query position
-    const int n_x = x ? n_b : n_a;
+    const int x0 = x ? b0 : a0, x1 = x ? b1 : a1;       // this tile's K/V tiles [x0, x1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + x * BLOCK_N;
     const uint32_t tO = tmem + lane_off + kTmemO + x * D;
@@ -322,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l = 0.f;         // sum of 2^(scaled score - m) over the keys seen so far
     bool ok = true;
 
-    for (int j = 0; j < n_x; ++j) {
-      if (!ptx::wait_bounded(bar(BAR_S_FULL + x), j & 1, abort_p, kWaitLimitNs)) {
+    for (int j = x0; j < x1; ++j) {
+      if (!ptx::wait_bounded(bar(BAR_S_FULL + x), (j - x0) & 1, abort_p, kWaitLimitNs)) {
         ok = false;
         break;
       }
@@ -348,11 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < BLOCK_N; t += 2)
           ptx::mul2(s[t], s[t + 1], s[t], s[t + 1], scale_log2, scale_log2);
       }
-      if ((causal && k0 + BLOCK_N - 1 > qt * BLOCK_M) || k0 + BLOCK_N > N) {
-        const int lim = (causal ? min(q_idx + 1, N) : N) - k0;   // keys k0 + [0, lim) allowed
+      if (!mask.tile_full(qt, j)) {
+        // keys k0 + [lo, hi) are allowed for this row
+        const int lo = mask.lo(q_idx) - k0, hi = mask.hi(q_idx) - k0;
 #pragma unroll
         for (int t = 0; t < BLOCK_N; ++t)
-          if (t >= lim) s[t] = -INFINITY;
+          if (t < lo || t >= hi) s[t] = -INFINITY;
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -401,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l += rs0 + rs1;
 
-      if (rescale && j > 0) {
+      if (rescale && j > x0) {
         // P_x(j-1) V_{j-1} has completed: it was issued before S_x(j).
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -420,7 +466,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------- epilogue
-    if (ok && ptx::wait_bounded(bar(BAR_O_DONE + x), (n_x - 1) & 1, abort_p, kWaitLimitNs)) {
+    if (x1 <= x0) {
+      // No row of this tile has an allowed key: O = 0 and LSE = -inf (l = 0), no TMEM access.
+      if (q_idx < N) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(o_ptr) +
+                                              ((static_cast<int64_t>(b) * N + q_idx) * H + h) * D);
+#pragma unroll
+        for (int t = 0; t < D / 8; ++t) dst[t] = make_uint4(0, 0, 0, 0);
+        lse_ptr[(static_cast<int64_t>(b) * H + h) * N + q_idx] = -INFINITY;
+      }
+    } else if (ok && ptx::wait_bounded(bar(BAR_O_DONE + x), (x1 - x0 - 1) & 1, abort_p,
+                                       kWaitLimitNs)) {
       ptx::tc_fence_after_sync();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool valid = q_idx < N;
@@ -481,7 +537,8 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   const int heads_per_group =
       static_cast<int>(std::max(1ll, std::min(bh, (64ll << 20) / kv_bytes_per_head)));
   kernel<<<grid, kThreads, smem, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.o, p.lse, p.H, p.N,
-                                           p.causal, p.scale_log2, heads_per_group);
+                                           p.causal, p.scale_log2, heads_per_group,
+                                           p.window_left, p.window_right, p.seqlens_k);
   return cudaGetLastError();
 }
 

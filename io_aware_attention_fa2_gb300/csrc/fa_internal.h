@@ -24,6 +24,9 @@ struct FwdParams {
   float* lse;         // [B, H, N]
   int B, H, N, d;
   int causal;
+  int window_left;    // key j visible to query i only if j >= i - window_left (< 0: no bound)
+  int window_right;   // ... and j <= i + window_right (< 0: no bound)
+  const int* seqlens_k;  // device int32 [B]: keys at or past seqlens_k[b] are masked; or null
   int fp16;           // 0: bf16, 1: fp16
   float scale_log2;   // scale * log2(e)
 };
