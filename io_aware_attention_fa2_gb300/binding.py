@@ -30,7 +30,9 @@ class FaError(RuntimeError):
 
 
 def library_path() -> str:
-    return os.path.join(_HERE, "_build", LIB_NAME)
+    """The in-tree build, or the library named by FA_GB300_LIBRARY (another build of the same
+    sources, e.g. with different compile flags)."""
+    return os.environ.get("FA_GB300_LIBRARY") or os.path.join(_HERE, "_build", LIB_NAME)
 
 
 def load_library() -> ctypes.CDLL:

@@ -114,13 +114,21 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // j < len (the batch's key length), j <= i (causal), j >= i - left (left >= 0) and
 // j <= i + right (right >= 0). The allowed keys of one query form the interval [lo(i), hi(i)),
 // and lo, hi never decrease with i.
+// WINDOWED = false: no window and no per-batch key length (only causal and the ragged tail), so
+// those terms fold away at compile time.
+template <bool WINDOWED>
 struct KeyMask {
   int len, causal, left, right;
-  __device__ __forceinline__ int lo(int i) const { return left >= 0 ? max(0, i - left) : 0; }
+  __device__ __forceinline__ int lo(int i) const {
+    if constexpr (WINDOWED) return left >= 0 ? max(0, i - left) : 0;
+    return 0;
+  }
   __device__ __forceinline__ int hi(int i) const {
     int z = len;
     if (causal) z = min(z, i + 1);
-    if (right >= 0) z = min(z, i + right + 1);
+    if constexpr (WINDOWED) {
+      if (right >= 0) z = min(z, i + right + 1);
+    }
     return z;
   }
   // K/V tiles [j0, j1) that hold an allowed key of some row of Q tile qt (rows < N only);
@@ -137,15 +145,10 @@ struct KeyMask {
       j1 = (z + BLOCK_N - 1) / BLOCK_N;
     }
   }
-  // True when K/V tile j needs no per-element mask for any row of Q tile qt.
-  __device__ __forceinline__ bool tile_full(int qt, int j) const {
-    const int r0 = qt * BLOCK_M, k0 = j * BLOCK_N;
-    return k0 >= lo(r0 + BLOCK_M - 1) && k0 + BLOCK_N <= hi(r0);
-  }
 };
 
 // ---------------------------------------------------------------------------------------------
-template <int D, bool FP16>
+template <int D, bool FP16, bool WINDOWED>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -181,8 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = rem / g_size;
   const int qblk = causal ? num_qblk - 1 - r : r;
   const int b = bh / H, h = bh % H;
-  KeyMask mask;
-  mask.len = seqlens_k ? min(max(seqlens_k[b], 0), N) : N;
+  KeyMask<WINDOWED> mask;
+  mask.len = (WINDOWED && seqlens_k) ? min(max(seqlens_k[b], 0), N) : N;
   mask.causal = causal;
   mask.left = window_left;
   mask.right = window_right;
@@ -331,11 +334,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = (j - u0) % kStages;
         const bool next = j + 1 < u1;
         if (!wait_v(j)) { ok = false; break; }
-        if (next && !wait_k(j + 1)) { ok = false; break; }
         if (on_a(j)) {
           if (!wait(BAR_P_FULL + 0, (j - a0) & 1)) { ok = false; break; }
           issue_pv(0, j, j == a0);
         }
+        if (next && !wait_k(j + 1)) { ok = false; break; }
         if (on_a(j + 1)) issue_s(0, j + 1);
         if (on_b(j)) {
           if (!wait(BAR_P_FULL + 1, (j - b0) & 1)) { ok = false; break; }
@@ -363,6 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + x * BLOCK_N;
     const uint32_t tO = tmem + lane_off + kTmemO + x * D;
     const bool scale_pos = scale_log2 > 0.f;
+    // This row's allowed keys [row_lo, row_hi); a K/V tile starting at k0 needs no per-element
+    // mask when full_lo <= k0 and k0 + BLOCK_N <= full_hi (inside every row's interval).
+    const int row_lo = mask.lo(q_idx), row_hi = mask.hi(q_idx);
+    const int full_lo = mask.lo(qt * BLOCK_M + BLOCK_M - 1), full_hi = mask.hi(qt * BLOCK_M);
     float m = -INFINITY;   // exponent offset in use, log2 units of scaled scores
     float l = 0.f;         // sum of 2^(scaled score - m) over the keys seen so far
     bool ok = true;
@@ -393,12 +400,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < BLOCK_N; t += 2)
           ptx::mul2(s[t], s[t + 1], s[t], s[t + 1], scale_log2, scale_log2);
       }
-      if (!mask.tile_full(qt, j)) {
-        // keys k0 + [lo, hi) are allowed for this row
-        const int lo = mask.lo(q_idx) - k0, hi = mask.hi(q_idx) - k0;
+      if (k0 < full_lo || k0 + BLOCK_N > full_hi) {
+        const int lo = row_lo - k0, hi = row_hi - k0;   // keys k0 + [lo, hi) are allowed
+        if constexpr (WINDOWED) {
 #pragma unroll
-        for (int t = 0; t < BLOCK_N; ++t)
-          if (t < lo || t >= hi) s[t] = -INFINITY;
+          for (int t = 0; t < BLOCK_N; ++t)
+            if (t < lo || t >= hi) s[t] = -INFINITY;
+        } else {
+#pragma unroll
+          for (int t = 0; t < BLOCK_N; ++t)
+            if (t >= hi) s[t] = -INFINITY;
+        }
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -522,9 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool FP16>
+template <int D, bool FP16, bool WINDOWED>
 cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
-  auto kernel = fa_fwd_kernel<D, FP16>;
+  auto kernel = fa_fwd_kernel<D, FP16, WINDOWED>;
   const size_t smem = SmemLayout<D>::kDynamic;
   cudaError_t err =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -552,9 +564,18 @@ long long fwd_num_ctas(int B, int H, int N) {
   return static_cast<long long>(B) * H * ((N + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M));
 }
 
+template <bool WINDOWED>
+cudaError_t launch_dtype(const FwdParams& p, cudaStream_t stream) {
+  if (p.d == 64)
+    return p.fp16 ? launch_impl<64, true, WINDOWED>(p, stream)
+                  : launch_impl<64, false, WINDOWED>(p, stream);
+  return p.fp16 ? launch_impl<128, true, WINDOWED>(p, stream)
+                : launch_impl<128, false, WINDOWED>(p, stream);
+}
+
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
-  if (p.d == 64) return p.fp16 ? launch_impl<64, true>(p, stream) : launch_impl<64, false>(p, stream);
-  return p.fp16 ? launch_impl<128, true>(p, stream) : launch_impl<128, false>(p, stream);
+  const bool windowed = p.window_left >= 0 || p.window_right >= 0 || p.seqlens_k != nullptr;
+  return windowed ? launch_dtype<true>(p, stream) : launch_dtype<false>(p, stream);
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t stream, int* value) {
