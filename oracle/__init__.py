@@ -79,9 +79,13 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
                                             vp, dbl, vp, vp]
     lib.oracle_attention_rows_masked.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i32, i64,
                                                  i64, vp, dbl, vp, i64, vp, vp]
+    lib.oracle_attention_qk.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, i32, i64, i64,
+                                        vp, dbl, vp, vp]
+    lib.oracle_attention_rows_qk.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, i32, i64,
+                                             i64, vp, dbl, vp, i64, vp, vp]
     for fn in (lib.oracle_decode, lib.oracle_attention, lib.oracle_attention_rows,
                lib.oracle_attention_masked, lib.oracle_attention_rows_masked,
-               lib.oracle_max_threads):
+               lib.oracle_attention_qk, lib.oracle_attention_rows_qk, lib.oracle_max_threads):
         fn.restype = i32
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -131,6 +135,15 @@ def decode(bits: np.ndarray, dtype: str, lib: ctypes.CDLL | None = None) -> np.n
     return out
 
 
+def _shapes(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape:
+        raise ValueError("q must be [B, Nq, H, d] and k, v one [B, Nk, H, d] shape")
+    B, Nq, H, d = q.shape
+    if k.shape[0] != B or k.shape[2] != H or k.shape[3] != d or k.shape[1] < Nq:
+        raise ValueError("k, v must be [B, Nk, H, d] with Nk >= Nq")
+    return B, Nq, k.shape[1], H, d
+
+
 def _lengths(seqlens_k, B):
     if seqlens_k is None:
         return None, None
@@ -145,25 +158,25 @@ def attention(q, k, v, causal: bool, scale: float, dtype: str | None = None,
     """Plain fp64 attention over [B, N, H, d] inputs.
 
     ``dtype`` None: q, k, v are real arrays (converted to float64). ``dtype`` "bf16"/"fp16":
-    they are uint16 bit patterns of that type. ``window`` = (left, right): key j is allowed
-    for query i only if j >= i - left (left >= 0) and j <= i + right (right >= 0); -1 means
-    no bound. ``seqlens_k``: optional per-batch key lengths (keys at or past the length do not
-    exist). Rows with no allowed key get O = 0 and LSE = -inf. Returns (o [B,N,H,d] float64,
-    lse [B,H,N] float64). ``scale`` is used exactly as given.
+    they are uint16 bit patterns of that type. q is [B, Nq, H, d], k and v [B, Nk, H, d] with
+    Nk >= Nq; the queries are the last Nq positions (query i sits at position i + Nk - Nq).
+    ``window`` = (left, right): key j is allowed for the query at position p only if
+    j >= p - left (left >= 0) and j <= p + right (right >= 0); -1 means no bound; causal means
+    j <= p. ``seqlens_k``: optional per-batch key lengths (keys at or past the length do not
+    exist). Rows with no allowed key get O = 0 and LSE = -inf. Returns (o [B,Nq,H,d] float64,
+    lse [B,H,Nq] float64). ``scale`` is used exactly as given.
     """
     lib = lib or load()
     kind, (q, k, v) = _kind_and_arrays(q, k, v, dtype)
-    if q.ndim != 4 or k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must share one [B, N, H, d] shape")
-    B, N, H, d = q.shape
+    B, Nq, Nk, H, d = _shapes(q, k, v)
     lens, lens_ptr = _lengths(seqlens_k, B)
-    o = np.empty((B, N, H, d), dtype=np.float64)
-    lse = np.empty((B, H, N), dtype=np.float64)
-    rc = lib.oracle_attention_masked(_ptr(q), _ptr(k), _ptr(v), kind, B, H, N, d,
-                                     int(bool(causal)), int(window[0]), int(window[1]),
-                                     lens_ptr, float(scale), _ptr(o), _ptr(lse))
+    o = np.empty((B, Nq, H, d), dtype=np.float64)
+    lse = np.empty((B, H, Nq), dtype=np.float64)
+    rc = lib.oracle_attention_qk(_ptr(q), _ptr(k), _ptr(v), kind, B, H, Nq, Nk, d,
+                                 int(bool(causal)), int(window[0]), int(window[1]), lens_ptr,
+                                 float(scale), _ptr(o), _ptr(lse))
     if rc:
-        raise RuntimeError("oracle_attention_masked failed: %d" % rc)
+        raise RuntimeError("oracle_attention_qk failed: %d" % rc)
     return o, lse
 
 
@@ -173,15 +186,15 @@ def attention_rows(q, k, v, rows, causal: bool, scale: float, dtype: str | None 
     triples, shape [R, 3]. Returns (o_rows [R, d], lse_rows [R])."""
     lib = lib or load()
     kind, (q, k, v) = _kind_and_arrays(q, k, v, dtype)
-    B, N, H, d = q.shape
+    B, Nq, Nk, H, d = _shapes(q, k, v)
     lens, lens_ptr = _lengths(seqlens_k, B)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
     o = np.empty((rows.shape[0], d), dtype=np.float64)
     lse = np.empty((rows.shape[0],), dtype=np.float64)
-    rc = lib.oracle_attention_rows_masked(_ptr(q), _ptr(k), _ptr(v), kind, B, H, N, d,
-                                          int(bool(causal)), int(window[0]), int(window[1]),
-                                          lens_ptr, float(scale), _ptr(rows), rows.shape[0],
-                                          _ptr(o), _ptr(lse))
+    rc = lib.oracle_attention_rows_qk(_ptr(q), _ptr(k), _ptr(v), kind, B, H, Nq, Nk, d,
+                                      int(bool(causal)), int(window[0]), int(window[1]),
+                                      lens_ptr, float(scale), _ptr(rows), rows.shape[0],
+                                      _ptr(o), _ptr(lse))
     if rc:
-        raise RuntimeError("oracle_attention_rows_masked failed: %d" % rc)
+        raise RuntimeError("oracle_attention_rows_qk failed: %d" % rc)
     return o, lse

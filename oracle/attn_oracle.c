@@ -26,9 +26,14 @@
  *       j >= i - window_left (window_left >= 0) and j <= i + window_right (window_right >= 0).
  *       The allowed keys always form one interval [lo, hi). A row with no allowed key has
  *       O = 0 and LSE = -inf (the sum l is 0).
+ *   "FlashAttention V2 核心原理与架构设计" §5.1 (combining with FlashDecoding for long
+ *       sequences): queries may be fewer than keys (Nq <= Nk, e.g. decoding). The queries are
+ *       then the last Nq positions of the sequence: query i sits at position i + Nk - Nq, and
+ *       the causal and window bounds above are taken relative to that position.
  *
- * Layouts: q, k, v and o are [B, N, H, d] row-major (element (b, n, h, c) at
- * ((b*N + n)*H + h)*d + c); lse is [B, H, N]; the optional key lengths are int32 [B].
+ * Layouts: q and o are [B, Nq, H, d], k and v [B, Nk, H, d], row-major (element (b, n, h, c)
+ * at ((b*N + n)*H + h)*d + c with N the tensor's own length); lse is [B, H, Nq]; the optional
+ * key lengths are int32 [B].
  *
  * There is no blocking, fusion or reordering here: one (b, h, i) row at a time, the three
  * passes in order. Rows are independent, so OpenMP spreads rows over host cores.
@@ -81,23 +86,24 @@ int oracle_decode(const uint16_t* bits, int64_t n, int kind, double* out) {
     return 0;
 }
 
-/* The keys query i may attend to: [lo, hi). `len_b` is the batch's key length. */
-static void key_range(int64_t i, int causal, int64_t wl, int64_t wr, int64_t len_b,
+/* The keys query i may attend to: [lo, hi). `len_b` is the batch's key length; `pos` is the
+ * query's position in the key sequence (i + Nk - Nq). */
+static void key_range(int64_t pos, int causal, int64_t wl, int64_t wr, int64_t len_b,
                       int64_t* lo, int64_t* hi) {
     int64_t a = 0, z = len_b;
-    if (causal && i + 1 < z) z = i + 1;
-    if (wl >= 0 && i - wl > a) a = i - wl;
-    if (wr >= 0 && i + wr + 1 < z) z = i + wr + 1;
+    if (causal && pos + 1 < z) z = pos + 1;
+    if (wl >= 0 && pos - wl > a) a = pos - wl;
+    if (wr >= 0 && pos + wr + 1 < z) z = pos + wr + 1;
     *lo = a;
     *hi = z;
 }
 
-/* One output row: query i of head (b, h) over keys [lo, hi). `s` is scratch of >= N doubles. */
+/* One output row: query i of head (b, h) over keys [lo, hi). `s` is scratch of >= Nk doubles. */
 static void attention_row(const void* q, const void* k, const void* v, int kind,
-                          int64_t N, int64_t H, int64_t d, int64_t lo, int64_t hi, double scale,
-                          int64_t b, int64_t h, int64_t i, double* s, double* o_row,
-                          double* lse_out) {
-    const int64_t q_off = ((b * N + i) * H + h) * d;
+                          int64_t Nq, int64_t Nk, int64_t H, int64_t d, int64_t lo, int64_t hi,
+                          double scale, int64_t b, int64_t h, int64_t i, double* s,
+                          double* o_row, double* lse_out) {
+    const int64_t q_off = ((b * Nq + i) * H + h) * d;
     if (lo >= hi) {             /* no key allowed: O = 0, LSE = -inf */
         for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
         *lse_out = -INFINITY;
@@ -106,7 +112,7 @@ static void attention_row(const void* q, const void* k, const void* v, int kind,
 
     /* Step 1: S[i, j] = scale * <q_i, k_j>. */
     for (int64_t j = lo; j < hi; ++j) {
-        const int64_t k_off = ((b * N + j) * H + h) * d;
+        const int64_t k_off = ((b * Nk + j) * H + h) * d;
         double dot = 0.0;
         for (int64_t c = 0; c < d; ++c) dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);
         s[j] = scale * dot;
@@ -127,7 +133,7 @@ static void attention_row(const void* q, const void* k, const void* v, int kind,
     /* Step 3: O[i, :] = P[i, :] V. */
     for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
     for (int64_t j = lo; j < hi; ++j) {
-        const int64_t v_off = ((b * N + j) * H + h) * d;
+        const int64_t v_off = ((b * Nk + j) * H + h) * d;
         for (int64_t c = 0; c < d; ++c) o_row[c] += s[j] * elem(v, kind, v_off + c);
     }
 
@@ -141,26 +147,27 @@ static int64_t batch_key_length(const int32_t* seqlens_k, int64_t b, int64_t N) 
 }
 
 static int check_args(const void* q, const void* k, const void* v, int kind, int64_t B,
-                      int64_t H, int64_t N, int64_t d) {
+                      int64_t H, int64_t Nq, int64_t Nk, int64_t d) {
     if (!q || !k || !v) return -1;
     if (kind != ORACLE_F64 && kind != ORACLE_BF16 && kind != ORACLE_FP16) return -2;
-    if (B < 1 || H < 1 || N < 1 || d < 1) return -3;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < Nq || d < 1) return -3;
     return 0;
 }
 
-/* Full attention with the general mask: o [B, N, H, d], lse [B, H, N]. */
-int oracle_attention_masked(const void* q, const void* k, const void* v, int kind, int64_t B,
-                            int64_t H, int64_t N, int64_t d, int causal, int64_t window_left,
-                            int64_t window_right, const int32_t* seqlens_k, double scale,
-                            double* o, double* lse) {
-    int rc = check_args(q, k, v, kind, B, H, N, d);
+/* Full attention, Nq queries against Nk >= Nq keys, general mask: o [B, Nq, H, d],
+ * lse [B, H, Nq]. */
+int oracle_attention_qk(const void* q, const void* k, const void* v, int kind, int64_t B,
+                        int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                        int64_t window_left, int64_t window_right, const int32_t* seqlens_k,
+                        double scale, double* o, double* lse) {
+    int rc = check_args(q, k, v, kind, B, H, Nq, Nk, d);
     if (rc) return rc;
     if (!o || !lse) return -1;
-    const int64_t rows = B * H * N;
+    const int64_t rows = B * H * Nq;
     int failed = 0;
 #pragma omp parallel
     {
-        double* s = (double*)malloc((size_t)N * sizeof(double));
+        double* s = (double*)malloc((size_t)Nk * sizeof(double));
         if (!s) {
 #pragma omp atomic write
             failed = 1;
@@ -168,12 +175,12 @@ int oracle_attention_masked(const void* q, const void* k, const void* v, int kin
 #pragma omp for schedule(dynamic, 16)
             for (int64_t r = 0; r < rows; ++r) {
                 /* r enumerates (b, h, i) with i fastest */
-                const int64_t i = r % N, h = (r / N) % H, b = r / (N * H);
+                const int64_t i = r % Nq, h = (r / Nq) % H, b = r / (Nq * H);
                 int64_t lo, hi;
-                key_range(i, causal, window_left, window_right,
-                          batch_key_length(seqlens_k, b, N), &lo, &hi);
-                attention_row(q, k, v, kind, N, H, d, lo, hi, scale, b, h, i, s,
-                              o + ((b * N + i) * H + h) * d, lse + (b * H + h) * N + i);
+                key_range(i + Nk - Nq, causal, window_left, window_right,
+                          batch_key_length(seqlens_k, b, Nk), &lo, &hi);
+                attention_row(q, k, v, kind, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,
+                              o + ((b * Nq + i) * H + h) * d, lse + (b * H + h) * Nq + i);
             }
             free(s);
         }
@@ -181,29 +188,37 @@ int oracle_attention_masked(const void* q, const void* k, const void* v, int kin
     return failed ? -4 : 0;
 }
 
+int oracle_attention_masked(const void* q, const void* k, const void* v, int kind, int64_t B,
+                            int64_t H, int64_t N, int64_t d, int causal, int64_t window_left,
+                            int64_t window_right, const int32_t* seqlens_k, double scale,
+                            double* o, double* lse) {
+    return oracle_attention_qk(q, k, v, kind, B, H, N, N, d, causal, window_left, window_right,
+                               seqlens_k, scale, o, lse);
+}
+
 int oracle_attention(const void* q, const void* k, const void* v, int kind, int64_t B,
                      int64_t H, int64_t N, int64_t d, int causal, double scale, double* o,
                      double* lse) {
-    return oracle_attention_masked(q, k, v, kind, B, H, N, d, causal, -1, -1, 0, scale, o, lse);
+    return oracle_attention_qk(q, k, v, kind, B, H, N, N, d, causal, -1, -1, 0, scale, o, lse);
 }
 
 /* Selected rows: rows[3t..3t+2] = (b, h, i); o_rows [nrows, d], lse_rows [nrows]. */
-int oracle_attention_rows_masked(const void* q, const void* k, const void* v, int kind,
-                                 int64_t B, int64_t H, int64_t N, int64_t d, int causal,
-                                 int64_t window_left, int64_t window_right,
-                                 const int32_t* seqlens_k, double scale, const int64_t* rows,
-                                 int64_t nrows, double* o_rows, double* lse_rows) {
-    int rc = check_args(q, k, v, kind, B, H, N, d);
+int oracle_attention_rows_qk(const void* q, const void* k, const void* v, int kind, int64_t B,
+                             int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                             int64_t window_left, int64_t window_right,
+                             const int32_t* seqlens_k, double scale, const int64_t* rows,
+                             int64_t nrows, double* o_rows, double* lse_rows) {
+    int rc = check_args(q, k, v, kind, B, H, Nq, Nk, d);
     if (rc) return rc;
     if (!rows || !o_rows || !lse_rows || nrows < 0) return -1;
     for (int64_t t = 0; t < nrows; ++t) {
         const int64_t b = rows[3 * t], h = rows[3 * t + 1], i = rows[3 * t + 2];
-        if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= N) return -5;
+        if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= Nq) return -5;
     }
     int failed = 0;
 #pragma omp parallel
     {
-        double* s = (double*)malloc((size_t)N * sizeof(double));
+        double* s = (double*)malloc((size_t)Nk * sizeof(double));
         if (!s) {
 #pragma omp atomic write
             failed = 1;
@@ -212,9 +227,9 @@ int oracle_attention_rows_masked(const void* q, const void* k, const void* v, in
             for (int64_t t = 0; t < nrows; ++t) {
                 const int64_t b = rows[3 * t], h = rows[3 * t + 1], i = rows[3 * t + 2];
                 int64_t lo, hi;
-                key_range(i, causal, window_left, window_right,
-                          batch_key_length(seqlens_k, b, N), &lo, &hi);
-                attention_row(q, k, v, kind, N, H, d, lo, hi, scale, b, h, i, s,
+                key_range(i + Nk - Nq, causal, window_left, window_right,
+                          batch_key_length(seqlens_k, b, Nk), &lo, &hi);
+                attention_row(q, k, v, kind, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,
                               o_rows + t * d, lse_rows + t);
             }
             free(s);
@@ -223,12 +238,22 @@ int oracle_attention_rows_masked(const void* q, const void* k, const void* v, in
     return failed ? -4 : 0;
 }
 
+int oracle_attention_rows_masked(const void* q, const void* k, const void* v, int kind,
+                                 int64_t B, int64_t H, int64_t N, int64_t d, int causal,
+                                 int64_t window_left, int64_t window_right,
+                                 const int32_t* seqlens_k, double scale, const int64_t* rows,
+                                 int64_t nrows, double* o_rows, double* lse_rows) {
+    return oracle_attention_rows_qk(q, k, v, kind, B, H, N, N, d, causal, window_left,
+                                    window_right, seqlens_k, scale, rows, nrows, o_rows,
+                                    lse_rows);
+}
+
 int oracle_attention_rows(const void* q, const void* k, const void* v, int kind, int64_t B,
                           int64_t H, int64_t N, int64_t d, int causal, double scale,
                           const int64_t* rows, int64_t nrows, double* o_rows,
                           double* lse_rows) {
-    return oracle_attention_rows_masked(q, k, v, kind, B, H, N, d, causal, -1, -1, 0, scale,
-                                        rows, nrows, o_rows, lse_rows);
+    return oracle_attention_rows_qk(q, k, v, kind, B, H, N, N, d, causal, -1, -1, 0, scale,
+                                    rows, nrows, o_rows, lse_rows);
 }
 
 int oracle_max_threads(void) {

@@ -78,23 +78,27 @@ def blockwise_attention(q, k, v, Br: int, Bc: int, causal: bool, scale: float,
                         window=(-1, -1), kv_len=None):
     """Tiled attention with online softmax, fp64, for one head.
 
-    q, k, v: [N, d] float arrays. ``window`` = (left, right) bounds the keys a query sees
-    (j >= i - left, j <= i + right; -1 = no bound); ``kv_len`` (default N): keys at or past it
+    q: [Nq, d], k, v: [Nk, d] float arrays with Nk >= Nq; query i sits at position
+    i + Nk - Nq. ``window`` = (left, right) bounds the keys a query at position p sees
+    (j >= p - left, j <= p + right; -1 = no bound); ``kv_len`` (default Nk): keys at or past it
     do not exist. K/V blocks with no allowed key for any row of the Q block are skipped.
-    Returns (O [N, d], LSE [N]) with LSE = m + ln l; rows with no allowed key get O = 0 and
+    Returns (O [Nq, d], LSE [Nq]) with LSE = m + ln l; rows with no allowed key get O = 0 and
     LSE = -inf.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
-    N, d = q.shape
+    Nq, d = q.shape
+    N = k.shape[0]
+    offset = N - Nq
     kv_len = N if kv_len is None else kv_len
     left, right = window
-    O = np.zeros((N, d))
-    LSE = np.zeros(N)
-    for i0 in range(0, N, Br):                        # outer loop: Q blocks
-        rows = np.arange(i0, min(i0 + Br, N))
+    O = np.zeros((Nq, d))
+    LSE = np.zeros(Nq)
+    for i0 in range(0, Nq, Br):                       # outer loop: Q blocks
+        rows = np.arange(i0, min(i0 + Br, Nq))
         Qi = q[rows]
+        pos = rows + offset                           # positions of these queries
         m = np.full(rows.size, -math.inf)
         l = np.zeros(rows.size)
         Oi = np.zeros((rows.size, d))
@@ -102,11 +106,11 @@ def blockwise_attention(q, k, v, Br: int, Bc: int, causal: bool, scale: float,
             cols = np.arange(j0, min(j0 + Bc, N))
             allowed = cols[None, :] < kv_len
             if causal:
-                allowed = allowed & (cols[None, :] <= rows[:, None])
+                allowed = allowed & (cols[None, :] <= pos[:, None])
             if left >= 0:
-                allowed = allowed & (cols[None, :] >= rows[:, None] - left)
+                allowed = allowed & (cols[None, :] >= pos[:, None] - left)
             if right >= 0:
-                allowed = allowed & (cols[None, :] <= rows[:, None] + right)
+                allowed = allowed & (cols[None, :] <= pos[:, None] + right)
             if not allowed.any():
                 continue                              # block fully masked: skipped
             S = np.where(allowed, scale * (Qi @ k[cols].T), -math.inf)   # local scores

@@ -378,3 +378,88 @@ ALL_PINS = [
     pin_tiled_algorithm, pin_torch_math_sdpa, pin_dtype_inputs, pin_padding_is_truncation,
     pin_sliding_window_brute_force, pin_window_special_cases, pin_tiled_algorithm_masks,
 ]
+
+
+def pin_fewer_queries_brute_force(lib):
+    """Nq < Nk (queries are the last Nq positions): equals the 60-digit brute force over the
+    allowed keys of position i + Nk - Nq, for causal, window and padding."""
+    rng = _rng(26)
+    B, Nq, Nk, H, d = 2, 3, 13, 2, 6
+    q = rng.standard_normal((B, Nq, H, d))
+    k, v = (rng.standard_normal((B, Nk, H, d)) for _ in range(2))
+    lens = [13, 9]
+    for causal, (left, right) in [(True, (-1, -1)), (False, (-1, -1)), (True, (4, -1)),
+                                  (False, (2, 1))]:
+        def allowed(b, i, j, causal=causal, left=left, right=right):
+            p = i + Nk - Nq
+            return (j < lens[b] and (not causal or j <= p) and (left < 0 or j >= p - left)
+                    and (right < 0 or j <= p + right))
+        o, lse = oracle.attention(q, k, v, causal, 0.5, lib=lib, window=(left, right),
+                                  seqlens_k=lens)
+        ob, lb = _brute_force_mp_qk(q, k, v, 0.5, allowed)
+        assert np.abs(o - ob).max() < 1e-12
+        fin = np.isfinite(lb)
+        assert np.array_equal(fin, np.isfinite(lse))
+        assert np.abs(lse[fin] - lb[fin]).max() < 1e-12
+
+
+def _brute_force_mp_qk(q, k, v, scale, allowed):
+    import mpmath
+    mp = mpmath.mp.clone()
+    mp.dps = 60
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    o = np.zeros((B, Nq, H, d))
+    lse = np.full((B, H, Nq), -math.inf)
+    for b in range(B):
+        for h in range(H):
+            for i in range(Nq):
+                js = [j for j in range(Nk) if allowed(b, i, j)]
+                if not js:
+                    continue
+                ws = [mp.exp(mp.mpf(scale) * mp.fsum(mp.mpf(float(q[b, i, h, c])) *
+                                                     mp.mpf(float(k[b, j, h, c]))
+                                                     for c in range(d))) for j in js]
+                den = mp.fsum(ws)
+                for c in range(d):
+                    o[b, i, h, c] = float(mp.fsum(w * mp.mpf(float(v[b, j, h, c]))
+                                                  for w, j in zip(ws, js)) / den)
+                lse[b, h, i] = float(mp.log(den))
+    return o, lse
+
+
+def pin_fewer_queries_are_last_rows(lib):
+    """Attention of the last Nq queries against all Nk keys equals the last Nq rows of the
+    square (Nq = Nk) attention whose final queries are those Nq, for every mask."""
+    rng = _rng(27)
+    B, Nk, H, d = 2, 37, 2, 8
+    q_full, k, v = (rng.standard_normal((B, Nk, H, d)) for _ in range(3))
+    for Nq in (1, 5, 37):
+        q = q_full[:, Nk - Nq:]
+        for causal, window, lens in [(True, (-1, -1), None), (False, (6, 3), [37, 20]),
+                                     (True, (10, -1), [30, 37])]:
+            o, lse = oracle.attention(q, k, v, causal, 0.3, lib=lib, window=window,
+                                      seqlens_k=lens)
+            of, lf = oracle.attention(q_full, k, v, causal, 0.3, lib=lib, window=window,
+                                      seqlens_k=lens)
+            assert np.array_equal(o, of[:, Nk - Nq:]) and np.array_equal(lse, lf[:, :, Nk - Nq:])
+
+
+def pin_tiled_algorithm_fewer_queries(lib):
+    """The tiled algorithm with Nq < Nk (query blocks at the end of the key sequence)
+    reaches the plain definition."""
+    rng = _rng(28)
+    Nq, Nk, d = 11, 40, 8
+    q = rng.standard_normal((1, Nq, 1, d))
+    k, v = (rng.standard_normal((1, Nk, 1, d)) for _ in range(2))
+    for causal, window in [(True, (-1, -1)), (False, (9, 2)), (True, (5, -1))]:
+        o, lse = oracle.attention(q, k, v, causal, 0.4, lib=lib, window=window)
+        for Br, Bc in [(4, 8), (16, 7)]:
+            ot, lt = oracle.blockwise_attention(q[0, :, 0], k[0, :, 0], v[0, :, 0], Br, Bc,
+                                                causal, 0.4, window=window)
+            assert np.abs(ot - o[0, :, 0]).max() < 1e-12
+            assert np.abs(lt - lse[0, 0]).max() < 1e-12
+
+
+ALL_PINS += [pin_fewer_queries_brute_force, pin_fewer_queries_are_last_rows,
+             pin_tiled_algorithm_fewer_queries]

@@ -14,15 +14,24 @@ MUTANTS = [
     ("wrong_sign_in_exp", "s[j] = exp(s[j] - m) / l;", "s[j] = exp(m - s[j]) / l;"),
     ("transposed_q_k", "dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);",
      "dot += elem(k, kind, q_off + c) * elem(q, kind, k_off + c);"),
-    ("query_row_for_value", "const int64_t v_off = ((b * N + j) * H + h) * d;",
-     "const int64_t v_off = ((b * N + i) * H + h) * d;"),
-    ("causal_excludes_diagonal", "if (causal && i + 1 < z) z = i + 1;",
-     "if (causal && i < z) z = i;"),
-    ("causal_off_by_one_extra", "if (causal && i + 1 < z) z = i + 1;",
-     "if (causal && i + 2 < z) z = i + 2;"),
-    ("window_left_off_by_one", "if (wl >= 0 && i - wl > a) a = i - wl;",
-     "if (wl >= 0 && i - wl + 1 > a) a = i - wl + 1;"),
-    ("window_right_ignored", "if (wr >= 0 && i + wr + 1 < z) z = i + wr + 1;", ""),
+    ("query_row_for_value", "const int64_t v_off = ((b * Nk + j) * H + h) * d;",
+     "const int64_t v_off = ((b * Nk + i) * H + h) * d;"),
+    ("causal_excludes_diagonal", "if (causal && pos + 1 < z) z = pos + 1;",
+     "if (causal && pos < z) z = pos;"),
+    ("causal_off_by_one_extra", "if (causal && pos + 1 < z) z = pos + 1;",
+     "if (causal && pos + 2 < z) z = pos + 2;"),
+    ("window_left_off_by_one", "if (wl >= 0 && pos - wl > a) a = pos - wl;",
+     "if (wl >= 0 && pos - wl + 1 > a) a = pos - wl + 1;"),
+    ("window_right_ignored", "if (wr >= 0 && pos + wr + 1 < z) z = pos + wr + 1;", ""),
+    ("query_position_not_offset",
+     "key_range(i + Nk - Nq, causal, window_left, window_right,\n"
+     "                          batch_key_length(seqlens_k, b, Nk), &lo, &hi);\n"
+     "                attention_row(q, k, v, kind, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,\n"
+     "                              o + ((b",
+     "key_range(i, causal, window_left, window_right,\n"
+     "                          batch_key_length(seqlens_k, b, Nk), &lo, &hi);\n"
+     "                attention_row(q, k, v, kind, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,\n"
+     "                              o + ((b"),
     ("padding_ignored", "if (!seqlens_k) return N;", "return N;"),
     ("empty_row_lse_zero", "*lse_out = -INFINITY;", "*lse_out = 0.0;"),
     ("scale_dropped", "s[j] = scale * dot;", "s[j] = dot;"),
@@ -30,17 +39,17 @@ MUTANTS = [
     ("lse_without_max", "*lse_out = m + log(l);", "*lse_out = log(l);"),
     ("lse_base2", "*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
     ("no_normalisation", "s[j] = exp(s[j] - m) / l;", "s[j] = exp(s[j] - m);"),
-    ("head_index_ignored", "const int64_t k_off = ((b * N + j) * H + h) * d;",
-     "const int64_t k_off = ((b * N + j) * H + 0) * d;"),
-    ("batch_index_ignored", "const int64_t q_off = ((b * N + i) * H + h) * d;",
-     "const int64_t q_off = ((0 * N + i) * H + h) * d;"),
+    ("head_index_ignored", "const int64_t k_off = ((b * Nk + j) * H + h) * d;",
+     "const int64_t k_off = ((b * Nk + j) * H + 0) * d;"),
+    ("batch_index_ignored", "const int64_t q_off = ((b * Nq + i) * H + h) * d;",
+     "const int64_t q_off = ((0 * Nq + i) * H + h) * d;"),
     ("max_over_prefix_only", "for (int64_t j = lo; j < hi; ++j)\n        if (s[j] > m)",
      "for (int64_t j = lo; j < lo + (hi - lo) / 2; ++j)\n        if (s[j] > m)"),
     ("fp16_bias_wrong", "ldexp((double)(1024 + mant), expo - 25)",
      "ldexp((double)(1024 + mant), expo - 24)"),
     ("fp16_subnormal_wrong", "ldexp((double)mant, -24)", "ldexp((double)mant, -25)"),
     ("bf16_shift_wrong", "(uint32_t)bits << 16", "(uint32_t)bits << 15"),
-    ("lse_stride_wrong", "lse + (b * H + h) * N + i", "lse + (b * H + h) * N + 0"),
+    ("lse_stride_wrong", "lse + (b * H + h) * Nq + i", "lse + (b * H + h) * Nq + 0"),
 ]
 
 
