@@ -47,13 +47,25 @@ KERNEL_SOURCES = ["io_aware_attention_fa2_gb300/csrc/fa_fwd_kernel.cu",
 
 
 def metric_flops(w) -> float:
-    f = 4.0 * w.B * w.H * w.N * w.N * w.d
-    return f / 2 if w.causal else f
+    """4*B*H*N^2*d (halved when causal) for Nq = Nk; with fewer queries than keys, 4*B*H*d per
+    visible (query, key) pair (causal: query i sees i + Nk - Nq + 1 keys)."""
+    if not w.Nk:
+        f = 4.0 * w.B * w.H * w.N * w.N * w.d
+        return f / 2 if w.causal else f
+    nq, nk = w.N, w.Nk
+    pairs = nq * (nk - nq) + nq * (nq + 1) / 2 if w.causal else nq * nk
+    return 4.0 * w.B * w.H * w.d * pairs
 
 
 def algorithmic_bytes(w) -> int:
     """Q, K, V read once, O written once (2 bytes each), LSE written once (4 bytes)."""
-    return 4 * w.B * w.H * w.N * w.d * 2 + w.B * w.H * w.N * 4
+    nk = w.n_keys
+    return (2 * w.N + 2 * nk) * w.B * w.H * w.d * 2 + w.B * w.H * w.N * 4
+
+
+def memory_bound(w) -> bool:
+    """Decoding-style workloads (a few queries per head) are bound by reading K and V."""
+    return metric_flops(w) / algorithmic_bytes(w) < 275.0
 
 
 def kernel_source_hash() -> str:
@@ -64,14 +76,19 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+FALLBACK_HBM_GBS = 6800.0
+
+
 def measured_peaks():
+    """(bf16 TFLOP/s burst, bf16 TFLOP/s sustained, HBM GB/s, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             p = json.load(f)
-        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+        return (float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)),
+                float(p.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured")
     except (OSError, KeyError, ValueError):
-        return FALLBACK_BF16_TFLOPS, 0.0, "fallback"
+        return FALLBACK_BF16_TFLOPS, 0.0, FALLBACK_HBM_GBS, "fallback"
 
 
 def traffic_record(workload: str):
@@ -293,12 +310,25 @@ def run_gpu(args, w):
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # Fewer queries than keys: the split-K/V forward, its workspace allocated up front.
+    num_splits = binding.splitkv_num_splits(w.B, w.H, w.N, w.n_keys) if w.Nk else 1
+    workspace = None
+    if w.Nk and num_splits > 1:
+        workspace = torch.empty(binding.splitkv_workspace_size(w.B, w.H, w.N, w.d, num_splits),
+                                dtype=torch.uint8, device=dev)
 
     # parity on sampled rows before timing (rank 0)
     parity = None
+    def call():
+        if w.Nk:
+            binding.fa_fwd_splitkv(q, k, v, o, lse, w.causal, w.scale, num_splits, workspace,
+                                   stream)
+        else:
+            binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+
     if rank == 0 and not args.no_check:
         import oracle
-        binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+        call()
         if binding.device_error(stream) != 0:
             raise RuntimeError("kernel wait timed out")
         rows = sample_rows(w.B, w.H, w.N, 8, seed=w.seed + 5)
@@ -319,7 +349,7 @@ def run_gpu(args, w):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
-        binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+        call()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -377,7 +407,7 @@ def run_gpu(args, w):
     e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
 
     if rank == 0:
-        peak, peak_sus, peak_src = measured_peaks()
+        peak, peak_sus, hbm_peak, peak_src = measured_peaks()
         achieved = flops / (kernel_ms * 1e-3) / 1e12
         line = {
             "metric": "attn fwd TFLOP/s (causal N=8K d=128 headline)" if w.name ==
@@ -391,25 +421,35 @@ def run_gpu(args, w):
                        "parallelism": "replicas x%d" % world},
             "pct_of_peak": 100.0 * achieved / peak,
             "peak_denominator": "%s bf16 dense %.1f TFLOP/s" % (peak_src, peak),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": "%s (burst)" % peak_src,
-                         "traffic": traffic_record(w.name),
-                         "algorithmic_bytes": algorithmic_bytes(w)},
+            "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak,
+                          "unit": "TFLOP/s", "frac": achieved / peak,
+                          "peak_source": "%s (burst)" % peak_src,
+                          "traffic": traffic_record(w.name),
+                          "algorithmic_bytes": algorithmic_bytes(w)}
+                         if not memory_bound(w) else
+                         {"bound": "hbm",
+                          "achieved": algorithmic_bytes(w) / (kernel_ms * 1e-3) / 1e9,
+                          "peak": hbm_peak, "unit": "GB/s",
+                          "frac": algorithmic_bytes(w) / (kernel_ms * 1e-3) / 1e9 / hbm_peak,
+                          "peak_source": "%s copy bandwidth" % peak_src,
+                          "traffic": traffic_record(w.name),
+                          "algorithmic_bytes": algorithmic_bytes(w)}),
+            "num_splits": num_splits,
+            "gpu_launches_per_step": 2 if num_splits > 1 else 1,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host),
                     "d2h_bytes_per_step": o_host.numel() * 2 + l_host.numel() * 4,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if num_splits > 1 else 1),
             "kernel_ms": {"mean": kernel_ms, "min": min(per_step_ms),
                           "max": max(per_step_ms)},
             "wall_s_timed_region": t_wall,
             "clocks": clocks.summary(),
             "parity": parity,
         }
-        if peak_sus:
+        if peak_sus and not memory_bound(w):
             line["roofline"]["frac_of_sustained"] = achieved / peak_sus
-        if args.vs_standard:
+        if args.vs_standard and not w.Nk:
             std_ms, o_std = time_standard_attention(q, k, v, w, min(args.steps, 20), flush,
                                                     stream)
             std = {"ms": std_ms, "tflops": flops / (std_ms * 1e-3) / 1e12,

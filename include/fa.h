@@ -31,6 +31,8 @@
 #ifndef FA_GB300_FA_H
 #define FA_GB300_FA_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -56,7 +58,8 @@ enum fa_status {
     FA_ERR_LAUNCH = -7,   /* the kernel launch failed (the CUDA error is not cleared) */
     FA_ERR_TIMEOUT = -8,  /* a kernel wait ran past its limit; outputs are undefined */
     FA_ERR_SCALE = -9,    /* scale is not finite */
-    FA_ERR_CUDA = -10     /* a CUDA runtime or driver query failed */
+    FA_ERR_CUDA = -10,    /* a CUDA runtime or driver query failed */
+    FA_ERR_WORKSPACE = -11  /* workspace smaller than fa_fwd_splitkv_workspace_size() */
 };
 
 /*
@@ -100,6 +103,40 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                   int H, int N, int d, int causal, int window_left, int window_right,
                   const int* seqlens_k, float scale, int dtype, fa_stream_t stream);
+
+/*
+ * fa_fwd_splitkv -- the forward with fewer queries than keys and with each (b, h, Q block)'s
+ * K/V range cut into num_splits parts computed by separate CTAs, then merged. This is the
+ * combination with FlashDecoding that "FlashAttention V2 核心原理与架构设计" §5.1 suggests for
+ * very long sequences: when B * H * ceil(Nq / 256) is small against the number of SMs (few
+ * heads, few queries, e.g. decoding), the parts fill the GPU. The merge applies the online-
+ * softmax rule of "FlashAttention 优化原理与实现要点解析" §4.2 to whole parts: with part s
+ * giving O_s (normalised by its own sum) and LSE_s, LSE = ln sum_s e^{LSE_s} and
+ * O = sum_s e^{LSE_s - LSE} O_s.
+ *
+ *   q, o       [B, Nq, H, d];  k, v  [B, Nk, H, d] with Nk >= Nq;  lse  [B, H, Nq] fp32
+ *              The queries are the last Nq positions of the sequence: query i sits at
+ *              position i + Nk - Nq, and causal / window bounds are relative to it (so Nq = 1
+ *              with causal sees every key: one decoding step).
+ *   num_splits 1..128 parts; 1 needs no workspace (workspace may then be NULL).
+ *   workspace  device memory of at least fa_fwd_splitkv_workspace_size(B, H, Nq, d,
+ *              num_splits) bytes, 16-byte aligned, owned by the caller; it must not overlap any
+ *              input or output. It holds the parts (fp32) until the merge kernel, enqueued on
+ *              the same stream, has read them; calls that share a workspace must not overlap.
+ *   everything else as in fa_fwd_masked.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int H, int Nq, int Nk, int d, int causal, int window_left, int window_right,
+                   const int* seqlens_k, float scale, int dtype, int num_splits,
+                   void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Bytes of workspace fa_fwd_splitkv needs: B*H*Nq*num_splits*(d + 1)*4; 0 for one part. */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int d, int num_splits);
+
+/* A part count for fa_fwd_splitkv: 1 when the (b, h, Q block) units alone give every one of
+ * num_sms SMs a CTA; otherwise enough parts to do so, each keeping at least 4 K/V tiles of
+ * 128 keys, at most 128. */
+int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int num_sms);
 
 /* Static English text for a status code (never NULL). */
 const char* fa_error_string(int code);

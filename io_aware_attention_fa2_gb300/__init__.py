@@ -9,7 +9,9 @@ Importing the package does not load the CUDA library; the first call does, and r
 library has not been built (there is no fallback path).
 """
 from .binding import (FaError, attention_forward, available, device_error, error_string,
-                      fa_fwd, library_path, load_library)
+                      fa_fwd, fa_fwd_splitkv, library_path, load_library, splitkv_num_splits,
+                      splitkv_workspace_size)
 
 __all__ = ["FaError", "attention_forward", "available", "device_error", "error_string",
-           "fa_fwd", "library_path", "load_library"]
+           "fa_fwd", "fa_fwd_splitkv", "library_path", "load_library", "splitkv_num_splits",
+           "splitkv_workspace_size"]

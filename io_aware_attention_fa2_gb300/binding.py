@@ -52,6 +52,13 @@ def load_library() -> ctypes.CDLL:
             lib.fa_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                           vp, f32, i32, vp]
             lib.fa_fwd_masked.restype = i32
+            lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                           i32, vp, f32, i32, i32, vp, ctypes.c_size_t, vp]
+            lib.fa_fwd_splitkv.restype = i32
+            lib.fa_fwd_splitkv_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+            lib.fa_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
+            lib.fa_fwd_splitkv_num_splits.argtypes = [i32, i32, i32, i32, i32]
+            lib.fa_fwd_splitkv_num_splits.restype = i32
             lib.fa_error_string.argtypes = [i32]
             lib.fa_error_string.restype = ctypes.c_char_p
             lib.fa_get_device_error.argtypes = [vp]
@@ -140,20 +147,78 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None, window=(-1,
         raise FaError(rc, where)
 
 
+def splitkv_workspace_size(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:
+    """Bytes of workspace fa_fwd_splitkv needs (0 for one part)."""
+    return int(load_library().fa_fwd_splitkv_workspace_size(B, H, Nq, d, num_splits))
+
+
+def splitkv_num_splits(B: int, H: int, Nq: int, Nk: int, num_sms: int | None = None) -> int:
+    """The library's part count for fa_fwd_splitkv on a GPU with ``num_sms`` SMs (default:
+    the current device's)."""
+    if num_sms is None:
+        import torch
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return int(load_library().fa_fwd_splitkv_num_splits(B, H, Nq, Nk, num_sms))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, causal: bool, scale: float, num_splits: int,
+                   workspace=None, stream=None, window=(-1, -1), seqlens_k=None) -> None:
+    """Enqueue the split-K/V forward: q, o [B, Nq, H, d]; k, v [B, Nk, H, d] (Nk >= Nq; the
+    queries are the last Nq positions); lse float32 [B, H, Nq]. ``workspace``: a CUDA tensor of
+    at least ``splitkv_workspace_size`` bytes, or None to let PyTorch allocate one (it must
+    stay alive until the stream has run the call, which the caching allocator guarantees for
+    the current stream)."""
+    import torch
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be 4-D")
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    if k.shape != (B, Nk, H, d) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k, v must be [B, Nk, H, d] in q's dtype")
+    if o.shape != q.shape or o.dtype != q.dtype:
+        raise ValueError("o must match q")
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32:
+        raise ValueError("lse must be float32 [B, H, Nq]")
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    need = splitkv_workspace_size(B, H, Nq, d, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    lens_ptr = None
+    if seqlens_k is not None:
+        if (not seqlens_k.is_cuda or seqlens_k.dtype != torch.int32
+                or seqlens_k.shape != (B,) or not seqlens_k.is_contiguous()):
+            raise ValueError("seqlens_k must be a contiguous CUDA int32 tensor [B]")
+        lens_ptr = seqlens_k.data_ptr()
+    left, right = (int(w) for w in window)
+    rc = load_library().fa_fwd_splitkv(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d,
+        int(bool(causal)), left, right, lens_ptr, float(scale), _dtype_code(q), int(num_splits),
+        ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv")
+
+
 def device_error(stream=None) -> int:
     """Synchronise ``stream`` and return-and-clear the device error word (0 = none)."""
     return int(load_library().fa_get_device_error(_stream_handle(stream)))
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
-                      lse=None, stream=None, device=None, window=(-1, -1), seqlens_k=None):
+                      lse=None, stream=None, device=None, window=(-1, -1), seqlens_k=None,
+                      num_splits=None):
     """O, LSE = attention(q, k, v). The call a user makes.
 
     Device tensors are used in place. Host tensors (ideally pinned) are copied to ``device``
     (default cuda:0) on ``stream``, the kernel runs there, and O and LSE are copied back into
     host tensors, so the result is ready when the call returns. ``scale`` defaults to
     1/sqrt(d) rounded to fp32. ``window`` and ``seqlens_k`` (int32 [B], host or device) select
-    the padding and sliding-window masks (see ``fa_fwd``).
+    the padding and sliding-window masks (see ``fa_fwd``). k and v may be longer than q (the
+    queries are then the last positions, as when decoding); that case, or an explicit
+    ``num_splits``, runs the split-K/V forward (``num_splits`` None: the library's choice).
     """
     import math
 
@@ -161,12 +226,22 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     B, N, H, d = q.shape
     if scale is None:
         scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+    split = num_splits is not None or k.shape[1] != N
+
+    def run(qd, kd, vd, od, ld, st, lens):
+        if split:
+            ns = num_splits if num_splits is not None else splitkv_num_splits(
+                B, H, N, kd.shape[1])
+            fa_fwd_splitkv(qd, kd, vd, od, ld, causal, scale, ns, None, st, window, lens)
+        else:
+            fa_fwd(qd, kd, vd, od, ld, causal, scale, st, window, lens)
+
     if q.is_cuda:
         o = out if out is not None else torch.empty_like(q)
         ls = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32,
                                                      device=q.device)
         lens = None if seqlens_k is None else seqlens_k.to(q.device, torch.int32)
-        fa_fwd(q, k, v, o, ls, causal, scale, stream, window, lens)
+        run(q, k, v, o, ls, stream, lens)
         return o, ls
     dev = torch.device(device or "cuda:0")
     st = stream if stream is not None else torch.cuda.current_stream(dev)
@@ -175,7 +250,7 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         od = torch.empty_like(qd)
         ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         lens = None if seqlens_k is None else seqlens_k.to(dev, torch.int32, non_blocking=True)
-        fa_fwd(qd, kd, vd, od, ld, causal, scale, st, window, lens)
+        run(qd, kd, vd, od, ld, st, lens)
         o_host = out if out is not None else torch.empty(q.shape, dtype=q.dtype,
                                                          pin_memory=q.is_pinned())
         l_host = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32,

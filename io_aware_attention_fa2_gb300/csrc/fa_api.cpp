@@ -6,6 +6,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -84,7 +85,9 @@ const char* fa_error_string(int code) {
   switch (code) {
     case FA_OK: return "success";
     case FA_ERR_NULL: return "a required pointer is NULL";
-    case FA_ERR_SHAPE: return "unsupported shape (B, H, N >= 1; d in {64, 128}; size overflow)";
+    case FA_ERR_SHAPE:
+      return "unsupported shape (B, H, Nq >= 1; Nk >= Nq; d in {64, 128}; 1 <= num_splits <= "
+             "128; size overflow)";
     case FA_ERR_DTYPE: return "dtype is not FA_BF16 or FA_FP16";
     case FA_ERR_ALIGN:
       return "misaligned pointer (q, k, v, o: 16 bytes; lse, seqlens_k: 4 bytes)";
@@ -94,42 +97,59 @@ const char* fa_error_string(int code) {
     case FA_ERR_TIMEOUT: return "a kernel wait ran past its limit";
     case FA_ERR_SCALE: return "scale is not finite";
     case FA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case FA_ERR_WORKSPACE: return "workspace smaller than fa_fwd_splitkv_workspace_size()";
     default: return "unknown status";
   }
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-           int N, int d, int causal, float scale, int dtype, fa_stream_t stream) {
-  return fa_fwd_masked(q, k, v, o, lse, B, H, N, d, causal, -1, -1, nullptr, scale, dtype,
-                       stream);
-}
+}  // extern "C"
 
-int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                  int H, int N, int d, int causal, int window_left, int window_right,
-                  const int* seqlens_k, float scale, int dtype, fa_stream_t stream) {
+namespace {
+
+// Shared checks and launch of every forward entry point.
+int run_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Nq, int Nk, int d, int causal, int window_left, int window_right,
+                const int* seqlens_k, float scale, int dtype, int num_splits, void* workspace,
+                size_t workspace_bytes, fa_stream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return FA_ERR_SHAPE;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < Nq || (d != 64 && d != 128)) return FA_ERR_SHAPE;
+  if (num_splits < 1 || num_splits > fa::MAX_SPLITS) return FA_ERR_SHAPE;
   if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
   if (!isfinite(scale)) return FA_ERR_SCALE;
-  // Sizes: elements must fit int64; the grid is one CTA per (b, h, 256-row Q block), at most
-  // 2^31 - 1 CTAs.
+  // Sizes: elements must fit int64; the grid is one CTA per (b, h, 256-row Q block, K/V part),
+  // at most 2^31 - 1 CTAs.
   const uint64_t bh = (uint64_t)B * (uint64_t)H;
-  if (bh >= (1ull << 31) || bh * (uint64_t)((N + 255) / 256) >= (1ull << 31))
+  if (bh >= (1ull << 31) ||
+      bh * (uint64_t)((Nq + 255) / 256) * (uint64_t)num_splits >= (1ull << 31))
     return FA_ERR_SHAPE;
-  const uint64_t elems = bh * (uint64_t)N * (uint64_t)d;
-  if (elems > (1ull << 62) / 2) return FA_ERR_SHAPE;
-  const uint64_t t_bytes = elems * 2, lse_bytes = bh * (uint64_t)N * 4;
+  const uint64_t k_elems = bh * (uint64_t)Nk * (uint64_t)d;
+  if (k_elems > (1ull << 62) / 2) return FA_ERR_SHAPE;
+  const uint64_t q_bytes = bh * (uint64_t)Nq * d * 2, k_bytes = k_elems * 2;
+  const uint64_t lse_bytes = bh * (uint64_t)Nq * 4;
+  const uint64_t ws_need = fa_fwd_splitkv_workspace_size(B, H, Nq, d, num_splits);
+  if (num_splits > 1) {
+    if (!workspace) return FA_ERR_NULL;
+    if (workspace_bytes < ws_need) return FA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16) return FA_ERR_ALIGN;
+  }
   for (const void* p : {q, k, v, static_cast<const void*>(o)})
     if (reinterpret_cast<uintptr_t>(p) % 16) return FA_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(lse) % 4) return FA_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(seqlens_k) % 4) return FA_ERR_ALIGN;
-  if (seqlens_k && (overlaps(seqlens_k, (uint64_t)B * 4, o, t_bytes) ||
-                    overlaps(seqlens_k, (uint64_t)B * 4, lse, lse_bytes)))
-    return FA_ERR_ALIAS;
-  for (const void* in : {q, k, v})
-    if (overlaps(o, t_bytes, in, t_bytes) || overlaps(lse, lse_bytes, in, t_bytes))
-      return FA_ERR_ALIAS;
-  if (overlaps(o, t_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
+  struct Span { const void* p; uint64_t n; };
+  const Span ins[] = {{q, q_bytes}, {k, k_bytes}, {v, k_bytes},
+                      {seqlens_k, seqlens_k ? (uint64_t)B * 4 : 0}};
+  const Span outs[] = {{o, q_bytes}, {lse, lse_bytes},
+                       {num_splits > 1 ? workspace : nullptr, num_splits > 1 ? ws_need : 0}};
+  for (const Span& out : outs) {
+    if (!out.p) continue;
+    for (const Span& in : ins)
+      if (in.p && overlaps(out.p, out.n, in.p, in.n)) return FA_ERR_ALIAS;
+  }
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (outs[i].p && outs[j].p && overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n))
+        return FA_ERR_ALIAS;
 
   int device = 0;
   int rc = check_arch(&device);
@@ -137,14 +157,15 @@ int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* l
 
   fa::FwdParams p;
   const bool fp16 = dtype == FA_FP16;
-  if (!encode_bnhd(&p.tm_q, q, B, H, N, d, fp16) || !encode_bnhd(&p.tm_k, k, B, H, N, d, fp16) ||
-      !encode_bnhd(&p.tm_v, v, B, H, N, d, fp16))
+  if (!encode_bnhd(&p.tm_q, q, B, H, Nq, d, fp16) || !encode_bnhd(&p.tm_k, k, B, H, Nk, d, fp16) ||
+      !encode_bnhd(&p.tm_v, v, B, H, Nk, d, fp16))
     return FA_ERR_CUDA;
   p.o = o;
   p.lse = lse;
   p.B = B;
   p.H = H;
-  p.N = N;
+  p.Nq = Nq;
+  p.Nk = Nk;
   p.d = d;
   p.causal = causal ? 1 : 0;
   p.window_left = window_left < 0 ? -1 : window_left;
@@ -152,9 +173,55 @@ int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* l
   p.seqlens_k = seqlens_k;
   p.fp16 = fp16 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.num_splits = num_splits;
+  p.o_part = num_splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.lse_part = num_splits > 1 ? static_cast<float*>(workspace) + bh * (uint64_t)Nq * d * num_splits
+                              : nullptr;
   if (fa::launch_fwd(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FA_ERR_LAUNCH;
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+           int N, int d, int causal, float scale, int dtype, fa_stream_t stream) {
+  return run_forward(q, k, v, o, lse, B, H, N, N, d, causal, -1, -1, nullptr, scale, dtype, 1,
+                     nullptr, 0, stream);
+}
+
+int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int H, int N, int d, int causal, int window_left, int window_right,
+                  const int* seqlens_k, float scale, int dtype, fa_stream_t stream) {
+  return run_forward(q, k, v, o, lse, B, H, N, N, d, causal, window_left, window_right,
+                     seqlens_k, scale, dtype, 1, nullptr, 0, stream);
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int d, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || d < 1 || num_splits <= 1) return 0;
+  const uint64_t rows = (uint64_t)B * (uint64_t)H * (uint64_t)Nq * (uint64_t)num_splits;
+  return (size_t)(rows * (uint64_t)d * 4 + rows * 4);
+}
+
+int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int num_sms) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || num_sms < 1) return 1;
+  const long long units = (long long)B * H * ((Nq + 255) / 256);
+  const long long kv_tiles = (Nk + 127) / 128;
+  if (units >= num_sms) return 1;
+  // Enough parts to give every SM a CTA, each part keeping at least 4 K/V tiles.
+  long long splits = (num_sms + units - 1) / units;
+  splits = std::min<long long>(splits, std::max<long long>(1, kv_tiles / 4));
+  return (int)std::max<long long>(1, std::min<long long>(splits, fa::MAX_SPLITS));
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int H, int Nq, int Nk, int d, int causal, int window_left, int window_right,
+                   const int* seqlens_k, float scale, int dtype, int num_splits,
+                   void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return run_forward(q, k, v, o, lse, B, H, Nq, Nk, d, causal, window_left, window_right,
+                     seqlens_k, scale, dtype, num_splits, workspace, workspace_bytes, stream);
 }
 
 int fa_get_device_error(fa_stream_t stream) {

@@ -116,27 +116,29 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // and lo, hi never decrease with i.
 // WINDOWED = false: no window and no per-batch key length (only causal and the ragged tail), so
 // those terms fold away at compile time.
+// Query i sits at key position i + offset (offset = Nk - Nq: the queries are the last Nq
+// positions of the sequence, as when decoding against a longer key/value sequence).
 template <bool WINDOWED>
 struct KeyMask {
-  int len, causal, left, right;
+  int len, causal, left, right, offset;
   __device__ __forceinline__ int lo(int i) const {
-    if constexpr (WINDOWED) return left >= 0 ? max(0, i - left) : 0;
+    if constexpr (WINDOWED) return left >= 0 ? max(0, i + offset - left) : 0;
     return 0;
   }
   __device__ __forceinline__ int hi(int i) const {
     int z = len;
-    if (causal) z = min(z, i + 1);
+    if (causal) z = min(z, i + offset + 1);
     if constexpr (WINDOWED) {
-      if (right >= 0) z = min(z, i + right + 1);
+      if (right >= 0) z = min(z, i + offset + right + 1);
     }
     return z;
   }
-  // K/V tiles [j0, j1) that hold an allowed key of some row of Q tile qt (rows < N only);
+  // K/V tiles [j0, j1) that hold an allowed key of some row of Q tile qt (rows < Nq only);
   // j1 <= j0 when there is none.
-  __device__ __forceinline__ void tile_range(int qt, int N, int& j0, int& j1) const {
+  __device__ __forceinline__ void tile_range(int qt, int Nq, int& j0, int& j1) const {
     const int r0 = qt * BLOCK_M;
-    const int r_last = min(r0 + BLOCK_M, N) - 1;
-    const int a = lo(r0), z = r0 < N ? hi(r_last) : 0;
+    const int r_last = min(r0 + BLOCK_M, Nq) - 1;
+    const int a = lo(r0), z = r0 < Nq ? hi(r_last) : 0;
     if (z <= a) {
       j0 = 0;
       j1 = 0;
@@ -153,9 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
-                  float* __restrict__ lse_ptr, int H, int N, int causal, float scale_log2,
-                  int heads_per_group, int window_left, int window_right,
-                  const int* __restrict__ seqlens_k) {
+                  float* __restrict__ lse_ptr, int H, int Nq, int Nk, int causal,
+                  float scale_log2, int heads_per_group, int window_left, int window_right,
+                  const int* __restrict__ seqlens_k, int num_splits,
+                  float* __restrict__ o_part, float* __restrict__ lse_part) {
   using L = SmemLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_base_slot;
@@ -174,26 +177,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   // host so that a group's K and V stay resident in L2); within a group, units go Q block by
   // Q block across the group's heads, longest (causal) block first, so the CTAs in flight share
   // few heads and the long blocks start early.
-  const int num_qblk = (N + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M);
-  const int num_bh = gridDim.x / num_qblk;
-  const int group_units = heads_per_group * num_qblk;
+  // With num_splits > 1 every Q block's K/V range is cut into num_splits consecutive parts,
+  // one per CTA; the parts of a block are dispatched together.
+  const int num_qblk = (Nq + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M);
+  const int num_bh = gridDim.x / (num_qblk * num_splits);
+  const int group_units = heads_per_group * num_qblk * num_splits;
   const int g = static_cast<int>(blockIdx.x) / group_units;
   const int rem = static_cast<int>(blockIdx.x) % group_units;
   const int g_size = min(heads_per_group, num_bh - g * heads_per_group);
   const int bh = g * heads_per_group + rem % g_size;
-  const int r = rem / g_size;
+  const int r = rem / g_size / num_splits;
+  const int split = (rem / g_size) % num_splits;
   const int qblk = causal ? num_qblk - 1 - r : r;
   const int b = bh / H, h = bh % H;
   KeyMask<WINDOWED> mask;
-  mask.len = (WINDOWED && seqlens_k) ? min(max(seqlens_k[b], 0), N) : N;
+  mask.len = (WINDOWED && seqlens_k) ? min(max(seqlens_k[b], 0), Nk) : Nk;
   mask.causal = causal;
   mask.left = window_left;
   mask.right = window_right;
+  mask.offset = Nk - Nq;
   // K/V tile ranges of tile A and tile B ([x0, x1), empty when x1 <= x0; a0 <= b0 and
   // a1 <= b1 when both are non-empty) and their union [u0, u1), which the producer streams.
   int a0, a1, b0, b1;
-  mask.tile_range(kQTiles * qblk, N, a0, a1);
-  mask.tile_range(kQTiles * qblk + 1, N, b0, b1);
+  mask.tile_range(kQTiles * qblk, Nq, a0, a1);
+  mask.tile_range(kQTiles * qblk + 1, Nq, b0, b1);
+  if (num_splits > 1) {
+    // this CTA's part of the block's K/V tiles: [c0, c1)
+    const int w0 = a1 > a0 ? a0 : b0, w1 = b1 > b0 ? b1 : a1;
+    const int span = max(w1 - w0, 0);
+    const int c0 = w0 + span * split / num_splits, c1 = w0 + span * (split + 1) / num_splits;
+    a0 = max(a0, c0);
+    a1 = min(a1, c1);
+    b0 = max(b0, c0);
+    b1 = min(b1, c1);
+  }
   const bool a_any = a1 > a0, b_any = b1 > b0;
   const int u0 = a_any ? a0 : b0;
   const int u1 = b_any ? b1 : a1;
@@ -360,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;                       // TMEM lanes [32q, 32q+32)
     const int row = quarter * 32 + lane;                // query row within the tile
     const int qt = kQTiles * qblk + x;                  // global Q tile index
-    const int q_idx = qt * BLOCK_M + row;               // query position
+    const int q_idx = qt * BLOCK_M + row;               // query index (position - offset)
     const int x0 = x ? b0 : a0, x1 = x ? b1 : a1;       // this tile's K/V tiles [x0, x1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + x * BLOCK_N;
@@ -478,29 +495,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------- epilogue
+    // One split: O (input type) and LSE go straight to the outputs. Several splits: this
+    // CTA's part, normalised by its own l, goes to the fp32 workspace with its own LSE;
+    // fa_merge_kernel combines the parts.
+    const bool valid = q_idx < Nq;
+    const int64_t row_id = static_cast<int64_t>(bh) * Nq + q_idx;   // (b, h, q)
+    const int64_t part_row = static_cast<int64_t>(split) * num_bh * Nq + row_id;
+    uint16_t* out_row = static_cast<uint16_t*>(o_ptr) +
+                        ((static_cast<int64_t>(b) * Nq + q_idx) * H + h) * D;
     if (x1 <= x0) {
-      // No row of this tile has an allowed key: O = 0 and LSE = -inf (l = 0), no TMEM access.
-      if (q_idx < N) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(o_ptr) +
-                                              ((static_cast<int64_t>(b) * N + q_idx) * H + h) * D);
+      // No allowed key for this tile (in this part): O = 0 and LSE = -inf, no TMEM access.
+      if (valid) {
+        if (num_splits == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(out_row);
 #pragma unroll
-        for (int t = 0; t < D / 8; ++t) dst[t] = make_uint4(0, 0, 0, 0);
-        lse_ptr[(static_cast<int64_t>(b) * H + h) * N + q_idx] = -INFINITY;
+          for (int t = 0; t < D / 8; ++t) dst[t] = make_uint4(0, 0, 0, 0);
+          lse_ptr[row_id] = -INFINITY;
+        } else {
+          float4* dst = reinterpret_cast<float4*>(o_part + part_row * D);
+#pragma unroll
+          for (int t = 0; t < D / 4; ++t) dst[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+          lse_part[part_row] = -INFINITY;
+        }
       }
     } else if (ok && ptx::wait_bounded(bar(BAR_O_DONE + x), (x1 - x0 - 1) & 1, abort_p,
                                        kWaitLimitNs)) {
       ptx::tc_fence_after_sync();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool valid = q_idx < N;
-      uint16_t* out_row = static_cast<uint16_t*>(o_ptr) +
-                          ((static_cast<int64_t>(b) * N + q_idx) * H + h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t orr[32];
         ptx::tmem_ld_32x32b_x32(tO + c * 32, orr);
         ptx::tmem_wait_ld();
         ptx::reg_fence(orr);
-        if (valid) {
+        if (valid && num_splits == 1) {
           uint4* dst = reinterpret_cast<uint4*>(out_row + c * 32);
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
@@ -515,11 +543,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                               __uint_as_float(orr[8 * t + 7]) * inv_l);
             dst[t] = v;
           }
+        } else if (valid) {
+          float4* dst = reinterpret_cast<float4*>(o_part + part_row * D + c * 32);
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            dst[t] = make_float4(__uint_as_float(orr[4 * t + 0]) * inv_l,
+                                 __uint_as_float(orr[4 * t + 1]) * inv_l,
+                                 __uint_as_float(orr[4 * t + 2]) * inv_l,
+                                 __uint_as_float(orr[4 * t + 3]) * inv_l);
         }
       }
-      if (valid)
-        lse_ptr[(static_cast<int64_t>(b) * H + h) * N + q_idx] =
-            (m + __log2f(l)) * 0.69314718055994530942f;
+      if (valid) {
+        const float lse_row = (m + __log2f(l)) * 0.69314718055994530942f;
+        if (num_splits == 1)
+          lse_ptr[row_id] = lse_row;
+        else
+          lse_part[part_row] = lse_row;
+      }
     } else {
       record_timeout(abort_p);
     }
@@ -534,6 +574,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Merge of split K/V parts ("FlashAttention 优化原理与实现要点解析" §4.2: per-block statistics
+// merged into the global ones). Part s of a row holds O_s (normalised by its own l_s) and
+// LSE_s = m_s + ln l_s. Then LSE = ln sum_s e^{LSE_s} and O = sum_s e^{LSE_s - LSE} O_s.
+// One warp per (b, h, q) row; lane t owns D / 32 consecutive columns.
+template <int D, bool FP16>
+__global__ void __launch_bounds__(256)
+    fa_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                    void* __restrict__ o_ptr, float* __restrict__ lse_ptr, int H, int Nq,
+                    long long rows, int num_splits) {
+  constexpr int E = D / 32;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
+  if (row >= rows) return;
+  const int lane = threadIdx.x % 32;
+  float mx = -INFINITY;
+  for (int s = lane; s < num_splits; s += 32) mx = fmaxf(mx, lse_part[s * rows + row]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float sum = 0.f;
+  if (mx != -INFINITY)
+    for (int s = lane; s < num_splits; s += 32) sum += expf(lse_part[s * rows + row] - mx);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  const float lse_row = mx == -INFINITY ? -INFINITY : mx + logf(sum);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < num_splits; ++s) {
+      const float ls = lse_part[s * rows + row];
+      if (ls == -INFINITY) continue;
+      const float w = expf(ls - lse_row);
+      const float* src = o_part + (s * rows + row) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+    }
+  }
+  const long long bh = row / Nq;
+  const int q = static_cast<int>(row % Nq);
+  const long long b = bh / H, h = bh % H;
+  uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(o_ptr) +
+                                              ((b * Nq + q) * H + h) * D + lane * E);
+#pragma unroll
+  for (int e = 0; e < E; e += 2) dst[e / 2] = pack2<FP16>(acc[e], acc[e + 1]);
+  if (lane == 0) lse_ptr[row] = lse_row;
+}
+
 template <int D, bool FP16, bool WINDOWED>
 cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   auto kernel = fa_fwd_kernel<D, FP16, WINDOWED>;
@@ -541,16 +628,22 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   cudaError_t err =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  const long long num_qblk = (p.N + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M);
-  const dim3 grid(static_cast<unsigned>(num_qblk * p.B * p.H));
-  // Heads per dispatch group: K and V of a group within ~64 MiB of L2.
-  const long long kv_bytes_per_head = 4ll * p.N * p.d;
+  const long long num_qblk = (p.Nq + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M);
   const long long bh = static_cast<long long>(p.B) * p.H;
+  const dim3 grid(static_cast<unsigned>(num_qblk * bh * p.num_splits));
+  // Heads per dispatch group: K and V of a group within ~64 MiB of L2.
+  const long long kv_bytes_per_head = 4ll * p.Nk * p.d;
   const int heads_per_group =
       static_cast<int>(std::max(1ll, std::min(bh, (64ll << 20) / kv_bytes_per_head)));
-  kernel<<<grid, kThreads, smem, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.o, p.lse, p.H, p.N,
+  kernel<<<grid, kThreads, smem, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.o, p.lse, p.H, p.Nq, p.Nk,
                                            p.causal, p.scale_log2, heads_per_group,
-                                           p.window_left, p.window_right, p.seqlens_k);
+                                           p.window_left, p.window_right, p.seqlens_k,
+                                           p.num_splits, p.o_part, p.lse_part);
+  err = cudaGetLastError();
+  if (err != cudaSuccess || p.num_splits == 1) return err;
+  const long long rows = bh * p.Nq;
+  fa_merge_kernel<D, FP16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      p.o_part, p.lse_part, p.o, p.lse, p.H, p.Nq, rows, p.num_splits);
   return cudaGetLastError();
 }
 
@@ -560,8 +653,9 @@ size_t fwd_smem_bytes(int d) {
   return d == 64 ? SmemLayout<64>::kDynamic : SmemLayout<128>::kDynamic;
 }
 
-long long fwd_num_ctas(int B, int H, int N) {
-  return static_cast<long long>(B) * H * ((N + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M));
+long long fwd_num_ctas(int B, int H, int Nq, int num_splits) {
+  return static_cast<long long>(B) * H * ((Nq + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M)) *
+         num_splits;
 }
 
 template <bool WINDOWED>

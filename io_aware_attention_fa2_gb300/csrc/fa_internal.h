@@ -15,6 +15,8 @@ constexpr int BLOCK_N = 128;
 // A TMA box is BOX_ROWS tokens x BOX_COLS 16-bit elements (one 128-byte swizzle span per row).
 constexpr int BOX_ROWS = 128;
 constexpr int BOX_COLS = 64;
+// Most K/V parts a split forward may use.
+constexpr int MAX_SPLITS = 128;
 
 struct FwdParams {
   CUtensorMap tm_q;   // [B, N, H, d] viewed as 4-D (d, H, N, B); box (64, 1, 128, 1)
@@ -22,7 +24,11 @@ struct FwdParams {
   CUtensorMap tm_v;
   void* o;            // [B, N, H, d], same storage type as q
   float* lse;         // [B, H, N]
-  int B, H, N, d;
+  int B, H, d;
+  int Nq, Nk;         // queries (q, o, lse) and keys (k, v); Nk >= Nq, queries are the last Nq
+  int num_splits;     // >= 1: parts each (b, h, Q block)'s K/V range is cut into
+  float* o_part;      // num_splits > 1: fp32 [num_splits, B, H, Nq, d] partial O (workspace)
+  float* lse_part;    // num_splits > 1: fp32 [num_splits, B, H, Nq] partial LSE (workspace)
   int causal;
   int window_left;    // key j visible to query i only if j >= i - window_left (< 0: no bound)
   int window_right;   // ... and j <= i + window_right (< 0: no bound)
@@ -37,8 +43,8 @@ cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
 // Dynamic shared memory the forward kernel needs for head dimension d.
 size_t fwd_smem_bytes(int d);
 
-// Number of CTAs (one per 256-row Q block of every (b, h)) the forward kernel launches.
-long long fwd_num_ctas(int B, int H, int N);
+// Number of CTAs (one per 256-row Q block of every (b, h) and K/V part) the forward launches.
+long long fwd_num_ctas(int B, int H, int Nq, int num_splits);
 
 // Device error word of the current device: read (after synchronising `stream`) and clear.
 cudaError_t read_and_clear_device_error(cudaStream_t stream, int* value);

@@ -41,19 +41,24 @@ class Workload:
     q_scale: float = 1.0
     k_outlier_frac: float = 0.0
     k_outlier_scale: float = 1.0
+    Nk: int = 0           # keys (and values); 0 means N. Queries are then the last N positions.
 
     @property
     def scale(self) -> float:
         return softmax_scale(self.d)
+
+    @property
+    def n_keys(self) -> int:
+        return self.Nk or self.N
 
     def describe(self) -> str:
         extra = ""
         if self.q_scale != 1.0 or self.k_outlier_frac:
             extra = ", Q x%g, %g%% of K rows x%g" % (self.q_scale, 100 * self.k_outlier_frac,
                                                       self.k_outlier_scale)
-        return "B=%d H=%d N=%d d=%d %s %s%s" % (self.B, self.H, self.N, self.d, self.dtype,
-                                                "causal" if self.causal else "non-causal",
-                                                extra)
+        n = ("N=%d" % self.N) if not self.Nk else ("Nq=%d Nk=%d" % (self.N, self.Nk))
+        return "B=%d H=%d %s d=%d %s %s%s" % (self.B, self.H, n, self.d, self.dtype,
+                                              "causal" if self.causal else "non-causal", extra)
 
 
 # The five workloads (the second one in both mask modes). Sizes, types and input statistics
@@ -71,6 +76,10 @@ WORKLOADS = {
     # heads are not stated there, 2 x 16 is used).
     "n1k_d128": Workload("n1k_d128", 2, 16, 1024, 128, "bf16", False, 6000),
     "n8k_d128": Workload("n8k_d128", 2, 16, 8192, 128, "bf16", False, 7000),
+    # One decoding step against a long sequence (the FlashDecoding case the pages mention for
+    # N > 32K): 1 query per (b, h) attends to 65536 cached keys.
+    "decode_nk64k_d128": Workload("decode_nk64k_d128", 4, 32, 1, 128, "bf16", True, 8000,
+                                  Nk=65536),
 }
 
 
@@ -99,21 +108,23 @@ def normal(shape, seed: int) -> np.ndarray:
 
 
 def make_qkv(B: int, H: int, N: int, d: int, dtype: str, seed: int, q_scale: float = 1.0,
-             k_outlier_frac: float = 0.0, k_outlier_scale: float = 1.0):
-    """Q, K, V as uint16 bit arrays of shape [B, N, H, d] following the recipe above."""
-    shape = (B, N, H, d)
-    q = normal(shape, seed)
+             k_outlier_frac: float = 0.0, k_outlier_scale: float = 1.0, Nk: int | None = None):
+    """Q [B, N, H, d] and K, V [B, Nk, H, d] (Nk defaults to N) as uint16 bit arrays following
+    the recipe above."""
+    Nk = N if not Nk else Nk
+    q = normal((B, N, H, d), seed)
+    shape = (B, Nk, H, d)
     if q_scale != 1.0:
         q *= q_scale
     qb = round_to_bits(q, dtype)
     del q
     k = normal(shape, seed + 1)
-    n_out = int(round(k_outlier_frac * N))
+    n_out = int(round(k_outlier_frac * Nk))
     if n_out > 0 and k_outlier_scale != 1.0:
         rng = np.random.Generator(np.random.PCG64(seed + 3))
         for b in range(B):
             for h in range(H):
-                pos = rng.choice(N, size=n_out, replace=False)
+                pos = rng.choice(Nk, size=n_out, replace=False)
                 k[b, pos, h, :] *= k_outlier_scale
     kb = round_to_bits(k, dtype)
     del k
@@ -124,7 +135,7 @@ def make_qkv(B: int, H: int, N: int, d: int, dtype: str, seed: int, q_scale: flo
 def make_workload(w: Workload):
     """Q, K, V bit arrays for a named workload."""
     return make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.q_scale, w.k_outlier_frac,
-                    w.k_outlier_scale)
+                    w.k_outlier_scale, Nk=w.Nk or None)
 
 
 def sample_rows(B: int, H: int, N: int, per_head: int, seed: int) -> np.ndarray:

@@ -39,7 +39,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_error_strings(lib):
-    for code in range(-10, 1):
+    for code in range(-11, 1):
         assert lib.fa_error_string(code)
     assert lib.fa_error_string(-8) == b"a kernel wait ran past its limit"
     assert lib.fa_error_string(12345) == b"unknown status"
@@ -78,3 +78,37 @@ def test_valid_arguments_without_gpu_fail_in_device_query(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; the GPU tests cover real launches")
     assert _call(lib) in (FA_ERR_CUDA, FA_ERR_ARCH)
+
+
+def _split(lib, q=0x10000, k=0x20000, v=0x30000, o=0x40000, lse=0x50000, B=1, H=1, Nq=16,
+           Nk=128, d=64, causal=0, wl=-1, wr=-1, lens=None, scale=0.125, dtype=0, splits=2,
+           ws=0x100000, ws_bytes=1 << 20):
+    # Fake, never dereferenced addresses: every case below fails a host-side check first.
+    return lib.fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, causal, wl, wr, lens, scale,
+                              dtype, splits, ws, ws_bytes, None)
+
+
+def test_splitkv_workspace_size_and_split_count(lib):
+    # [num_splits, B, H, Nq, d] fp32 parts + [num_splits, B, H, Nq] fp32 LSE
+    assert lib.fa_fwd_splitkv_workspace_size(2, 3, 5, 128, 4) == 4 * 2 * 3 * 5 * (128 + 1) * 4
+    assert lib.fa_fwd_splitkv_workspace_size(2, 3, 5, 128, 1) == 0
+    # enough (b, h, Q block) units for every SM: no split
+    assert lib.fa_fwd_splitkv_num_splits(2, 16, 8192, 8192, 152) == 1
+    # decoding, 4 x 8 heads, 64K keys: ceil(152 / 32) = 5 parts
+    assert lib.fa_fwd_splitkv_num_splits(4, 8, 1, 65536, 152) == 5
+    # few keys: at least 4 K/V tiles of 128 per part
+    assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 1024, 152) == 2
+    assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 100, 152) == 1
+    assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 1 << 30, 152) == 128
+
+
+def test_splitkv_host_side_checks(lib):
+    assert _split(lib, Nk=8) == FA_ERR_SHAPE                 # Nk < Nq
+    assert _split(lib, splits=0) == FA_ERR_SHAPE
+    assert _split(lib, splits=129) == FA_ERR_SHAPE
+    assert _split(lib, ws=0) == FA_ERR_NULL                  # parts need a workspace
+    assert _split(lib, ws_bytes=100) == -11                  # FA_ERR_WORKSPACE
+    assert _split(lib, ws=0x100008) == FA_ERR_ALIGN
+    assert _split(lib, ws=0x40000) == FA_ERR_ALIAS           # workspace over o
+    assert _split(lib, ws=0x20000) == FA_ERR_ALIAS           # workspace over k
+    assert lib.fa_error_string(-11) == b"workspace smaller than fa_fwd_splitkv_workspace_size()"
