@@ -138,6 +138,32 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int d, int num_splits
  * 128 keys, at most 128. */
 int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int num_sms);
 
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that cannot allocate device memory at
+ * call time: a plugin running inside a host that owns the whole device-memory budget, or a
+ * latency-critical loop where an allocation (and the synchronisation it may imply) is not
+ * acceptable. The pages have no counterpart of this entry point; it is a deployment aid.
+ *
+ * Instead of a caller-provided workspace it uses one 8 MiB (8 * 2^20 bytes) device buffer
+ * built into the library, which every GPU that loads the library keeps until the process
+ * exits. It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. The
+ * caller still passes q, k, v, o, lse (and seqlens_k) exactly as for fa_fwd_splitkv.
+ *
+ *   - Calls whose parts need more than 8 MiB (fa_fwd_splitkv_workspace_size(B, H, Nq, d,
+ *     num_splits) > 8 MiB) return FA_ERR_WORKSPACE and enqueue nothing; use fewer parts, or
+ *     fa_fwd_splitkv with a workspace of your own.
+ *   - The first call on each device looks up the buffer's device address (once, with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls on a device share the buffer, which keeps the last call's contents. Nothing in
+ *     it needs clearing: each call writes every part it reads. Calls that overlap on the GPU
+ *     (on different streams without ordering between them) race on the buffer.
+ *   - Every argument means what it means for fa_fwd_splitkv; the return codes are the same.
+ */
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int Nq, int Nk, int d, int causal, int window_left,
+                           int window_right, const int* seqlens_k, float scale, int dtype,
+                           int num_splits, fa_stream_t stream);
+
 /* Static English text for a status code (never NULL). */
 const char* fa_error_string(int code);
 

@@ -1,0 +1,71 @@
+// fa_noalloc.cu -- fa_fwd_splitkv_noalloc: the split-K/V forward with a workspace that lives
+// inside the library, for callers that cannot allocate device memory when they call.
+//
+// Who needs it: code that runs inside a host which owns the whole device-memory budget (a
+// plugin of a serving engine or framework that forbids allocations after start-up), and
+// latency-critical loops where an allocation, with the device synchronisation cudaMalloc may
+// imply, is not acceptable. Such callers still pass their own inputs and outputs; only the
+// scratch space for the K/V parts comes from here.
+//
+// The scratch is one file-scope device array, kNoAllocScratchBytes (8 MiB) large. Every GPU
+// that loads this library keeps it for the life of the process. All calls on a device share
+// it and it keeps the last call's contents; nothing in it has to start at zero, because the
+// attention kernel writes every part row (O and LSE) of the parts a call uses before the merge
+// kernel reads them. Calls whose work overlaps on the GPU (different streams, no ordering
+// between them) race on the array; order them on one stream or with events.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fa.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+
+// Host code must not use this name as a device address: on the host it only identifies the
+// symbol. Its device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device with
+// that device current. Returns FA_OK or FA_ERR_CUDA.
+int scratch_for_current_device(void** out) {
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+    return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_ptr[device]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+      return FA_ERR_CUDA;
+    g_scratch_ptr[device] = ptr;
+  }
+  *out = g_scratch_ptr[device];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int Nq, int Nk, int d, int causal, int window_left,
+                           int window_right, const int* seqlens_k, float scale, int dtype,
+                           int num_splits, fa_stream_t stream) {
+  // Size check first: nothing is touched when the parts would not fit the built-in buffer.
+  const size_t need = fa_fwd_splitkv_workspace_size(B, H, Nq, d, num_splits);
+  if (need > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const int rc = scratch_for_current_device(&scratch);
+  if (rc != FA_OK) return rc;
+  return fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, causal, window_left, window_right,
+                        seqlens_k, scale, dtype, num_splits, scratch, kNoAllocScratchBytes,
+                        stream);
+}
+
+}  // extern "C"
