@@ -31,7 +31,7 @@ from .softmax import (blockwise_attention, online_softmax, online_softmax_stream
                       softmax_three_pass)
 
 __all__ = [
-    "build", "load", "decode", "attention", "attention_rows", "max_threads",
+    "build", "load", "decode", "attention", "attention_rows", "attention_bwd", "max_threads",
     "softmax_three_pass", "online_softmax", "online_softmax_stream", "blockwise_attention",
     "KIND_F64", "KIND_BF16", "KIND_FP16",
 ]
@@ -83,6 +83,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
                                         vp, dbl, vp, vp]
     lib.oracle_attention_rows_qk.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, i32, i64,
                                              i64, vp, dbl, vp, i64, vp, vp]
+    lib.oracle_attention_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, i32, i64, i64,
+                                         vp, dbl, vp, vp, vp]
+    lib.oracle_attention_bwd.restype = i32
     for fn in (lib.oracle_decode, lib.oracle_attention, lib.oracle_attention_rows,
                lib.oracle_attention_masked, lib.oracle_attention_rows_masked,
                lib.oracle_attention_qk, lib.oracle_attention_rows_qk, lib.oracle_max_threads):
@@ -198,3 +201,25 @@ def attention_rows(q, k, v, rows, causal: bool, scale: float, dtype: str | None 
     if rc:
         raise RuntimeError("oracle_attention_rows_qk failed: %d" % rc)
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, causal: bool, scale: float, dtype: str | None = None,
+                  lib: ctypes.CDLL | None = None, window=(-1, -1), seqlens_k=None):
+    """Gradients (dq, dk, dv), float64 [B, N, H, d], of L = sum(dout * O) for the attention
+    ``attention(q, k, v, causal, scale, ...)`` (queries and keys share N). ``dout`` has q's
+    shape and, like q, k, v, is a real array (dtype None) or uint16 bit patterns of ``dtype``.
+    """
+    lib = lib or load()
+    kind, (q, k, v) = _kind_and_arrays(q, k, v, dtype)
+    _, (dout, _, _) = _kind_and_arrays(dout, dout, dout, dtype)
+    B, Nq, Nk, H, d = _shapes(q, k, v)
+    if Nq != Nk or dout.shape != q.shape:
+        raise ValueError("the backward takes one length N and dout shaped like q")
+    lens, lens_ptr = _lengths(seqlens_k, B)
+    dq, dk, dv = (np.empty((B, Nq, H, d), dtype=np.float64) for _ in range(3))
+    rc = lib.oracle_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), kind, B, H, Nq, d,
+                                  int(bool(causal)), int(window[0]), int(window[1]), lens_ptr,
+                                  float(scale), _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc:
+        raise RuntimeError("oracle_attention_bwd failed: %d" % rc)
+    return dq, dk, dv

@@ -263,3 +263,100 @@ int oracle_max_threads(void) {
     return 1;
 #endif
 }
+
+/*
+ * Backward of the same attention (the gradients the kept statistics serve: "FlashAttention
+ * V2 核心原理与架构设计" §2.3 keeps m and l for the backward pass). With L = sum dO . O for a given
+ * upstream gradient dO, the chain rule through S = scale Q K^T, P = softmax(S), O = P V gives
+ *   dV = P^T dO,   dP = dO V^T,   dS_ij = P_ij (dP_ij - D_i) with D_i = sum_j P_ij dP_ij,
+ *   dQ = scale dS K,   dK = scale dS^T Q.
+ * Keys outside a query's allowed interval have P_ij = 0 (so dS_ij = 0). Queries and keys share
+ * N here. Per (b, h) the N x N matrix P is materialised in fp64; no blocking. Layouts as the
+ * forward: q, k, v, dout and dq, dk, dv are [B, N, H, d].
+ */
+int oracle_attention_bwd(const void* q, const void* k, const void* v, const void* dout,
+                         int kind, int64_t B, int64_t H, int64_t N, int64_t d, int causal,
+                         int64_t window_left, int64_t window_right, const int32_t* seqlens_k,
+                         double scale, double* dq, double* dk, double* dv) {
+    int rc = check_args(q, k, v, kind, B, H, N, N, d);
+    if (rc) return rc;
+    if (!dout || !dq || !dk || !dv) return -1;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        const int64_t b = bh / H, h = bh % H;
+        double* P = (double*)calloc((size_t)(N * N), sizeof(double));
+        double* dS = (double*)calloc((size_t)(N * N), sizeof(double));
+        if (!P || !dS) {
+            free(P);
+            free(dS);
+#pragma omp atomic write
+            failed = 1;
+            continue;
+        }
+        const int64_t len_b = batch_key_length(seqlens_k, b, N);
+        /* P, row by row (three-pass softmax over the allowed keys) */
+        for (int64_t i = 0; i < N; ++i) {
+            int64_t lo, hi;
+            key_range(i, causal, window_left, window_right, len_b, &lo, &hi);
+            if (lo >= hi) continue;
+            const int64_t q_off = ((b * N + i) * H + h) * d;
+            double m = -INFINITY;
+            for (int64_t j = lo; j < hi; ++j) {
+                const int64_t k_off = ((b * N + j) * H + h) * d;
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c)
+                    dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);
+                P[i * N + j] = scale * dot;
+                if (P[i * N + j] > m) m = P[i * N + j];
+            }
+            double l = 0.0;
+            for (int64_t j = lo; j < hi; ++j) l += exp(P[i * N + j] - m);
+            for (int64_t j = lo; j < hi; ++j) P[i * N + j] = exp(P[i * N + j] - m) / l;
+        }
+        /* dP = dO V^T, D_i = sum_j P_ij dP_ij, dS = P (dP - D) */
+        for (int64_t i = 0; i < N; ++i) {
+            const int64_t o_off = ((b * N + i) * H + h) * d;
+            double Di = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                if (P[i * N + j] == 0.0) continue;
+                const int64_t v_off = ((b * N + j) * H + h) * d;
+                double dp = 0.0;
+                for (int64_t c = 0; c < d; ++c)
+                    dp += elem(dout, kind, o_off + c) * elem(v, kind, v_off + c);
+                dS[i * N + j] = dp;
+                Di += P[i * N + j] * dp;
+            }
+            for (int64_t j = 0; j < N; ++j) dS[i * N + j] = P[i * N + j] * (dS[i * N + j] - Di);
+        }
+        /* dQ = scale dS K */
+        for (int64_t i = 0; i < N; ++i) {
+            double* out = dq + ((b * N + i) * H + h) * d;
+            for (int64_t c = 0; c < d; ++c) out[c] = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                if (dS[i * N + j] == 0.0) continue;
+                const int64_t k_off = ((b * N + j) * H + h) * d;
+                for (int64_t c = 0; c < d; ++c) out[c] += dS[i * N + j] * elem(k, kind, k_off + c);
+            }
+            for (int64_t c = 0; c < d; ++c) out[c] *= scale;
+        }
+        /* dK = scale dS^T Q, dV = P^T dO */
+        for (int64_t j = 0; j < N; ++j) {
+            double* gk = dk + ((b * N + j) * H + h) * d;
+            double* gv = dv + ((b * N + j) * H + h) * d;
+            for (int64_t c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
+            for (int64_t i = 0; i < N; ++i) {
+                const int64_t row = ((b * N + i) * H + h) * d;
+                const double ds = dS[i * N + j], p = P[i * N + j];
+                if (ds != 0.0)
+                    for (int64_t c = 0; c < d; ++c) gk[c] += ds * elem(q, kind, row + c);
+                if (p != 0.0)
+                    for (int64_t c = 0; c < d; ++c) gv[c] += p * elem(dout, kind, row + c);
+            }
+            for (int64_t c = 0; c < d; ++c) gk[c] *= scale;
+        }
+        free(P);
+        free(dS);
+    }
+    return failed ? -4 : 0;
+}

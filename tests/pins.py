@@ -463,3 +463,70 @@ def pin_tiled_algorithm_fewer_queries(lib):
 
 ALL_PINS += [pin_fewer_queries_brute_force, pin_fewer_queries_are_last_rows,
              pin_tiled_algorithm_fewer_queries]
+
+
+# --------------------------------------------------------------------------------- backward
+def _loss(lib, q, k, v, dout, causal, scale, window=(-1, -1), lens=None):
+    o, _ = oracle.attention(q, k, v, causal, scale, lib=lib, window=window, seqlens_k=lens)
+    return float((o * dout).sum())
+
+
+def pin_bwd_finite_differences(lib):
+    """dQ, dK, dV equal central differences of L = sum(dO * O) computed with the forward
+    (which is pinned on its own), on random elements, for several masks."""
+    rng = _rng(30)
+    B, N, H, d = 2, 9, 2, 5
+    q, k, v, dout = (rng.standard_normal((B, N, H, d)) for _ in range(4))
+    for causal, window, lens in [(False, (-1, -1), None), (True, (-1, -1), None),
+                                 (True, (3, -1), [9, 6])]:
+        dq, dk, dv = oracle.attention_bwd(q, k, v, dout, causal, 0.45, lib=lib, window=window,
+                                          seqlens_k=lens)
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            for _ in range(12):
+                idx = tuple(int(rng.integers(0, n)) for n in x.shape)
+                h = 1e-5
+                x0 = x[idx]
+                x[idx] = x0 + h
+                lp = _loss(lib, q, k, v, dout, causal, 0.45, window, lens)
+                x[idx] = x0 - h
+                lm = _loss(lib, q, k, v, dout, causal, 0.45, window, lens)
+                x[idx] = x0
+                fd = (lp - lm) / (2 * h)
+                assert abs(fd - g[idx]) <= 1e-7 * max(1.0, abs(fd)), (name, causal, idx, fd, g[idx])
+
+
+def pin_bwd_identities(lib):
+    """Rows of P sum to 1, so sum over keys of dV = sum over queries of dO and sum over keys of
+    dK = 0 (softmax ignores a common shift); with all keys equal P does not depend on Q, so
+    dQ = 0; with N = 1, dV = dO and dQ = dK = 0."""
+    rng = _rng(31)
+    B, N, H, d = 2, 23, 3, 8
+    q, k, v, dout = (rng.standard_normal((B, N, H, d)) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv = oracle.attention_bwd(q, k, v, dout, causal, 0.3, lib=lib)
+        assert np.abs(dv.sum(axis=1) - dout.sum(axis=1)).max() < 1e-12
+        assert np.abs(dk.sum(axis=1)).max() < 1e-12
+        k_eq = np.broadcast_to(k[:, :1], k.shape).copy()
+        dq0, _, _ = oracle.attention_bwd(q, k_eq, v, dout, causal, 0.3, lib=lib)
+        assert np.abs(dq0).max() < 1e-13
+    q1, k1, v1, do1 = (x[:, :1] for x in (q, k, v, dout))
+    dq, dk, dv = oracle.attention_bwd(q1, k1, v1, do1, True, 0.3, lib=lib)
+    assert np.array_equal(dv, do1) and not dq.any() and not dk.any()
+
+
+def pin_bwd_matches_torch_autograd(lib):
+    """Third opinion: torch autograd through math attention in float64 on the CPU."""
+    import torch
+    rng = _rng(32)
+    B, N, H, d = 2, 17, 2, 8
+    q, k, v, dout = (rng.standard_normal((B, N, H, d)) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv = oracle.attention_bwd(q, k, v, dout, causal, 0.35, lib=lib)
+        t = [torch.from_numpy(x.copy()).permute(0, 2, 1, 3).requires_grad_() for x in (q, k, v)]
+        o = torch.nn.functional.scaled_dot_product_attention(*t, is_causal=causal, scale=0.35)
+        o.backward(torch.from_numpy(dout).permute(0, 2, 1, 3))
+        for g, ref in zip((dq, dk, dv), t):
+            assert np.abs(g - ref.grad.permute(0, 2, 1, 3).numpy()).max() < 1e-12
+
+
+ALL_PINS += [pin_bwd_finite_differences, pin_bwd_identities, pin_bwd_matches_torch_autograd]

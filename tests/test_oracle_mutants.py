@@ -12,8 +12,9 @@ MUTANTS = [
     ("dropped_max_shift", "l += exp(s[j] - m);", "l += exp(s[j]);"),
     ("normalise_without_shift", "s[j] = exp(s[j] - m) / l;", "s[j] = exp(s[j]) / l;"),
     ("wrong_sign_in_exp", "s[j] = exp(s[j] - m) / l;", "s[j] = exp(m - s[j]) / l;"),
-    ("transposed_q_k", "dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);",
-     "dot += elem(k, kind, q_off + c) * elem(q, kind, k_off + c);"),
+    ("transposed_q_k",
+     "for (int64_t c = 0; c < d; ++c) dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);",
+     "for (int64_t c = 0; c < d; ++c) dot += elem(k, kind, q_off + c) * elem(q, kind, k_off + c);"),
     ("query_row_for_value", "const int64_t v_off = ((b * Nk + j) * H + h) * d;",
      "const int64_t v_off = ((b * Nk + i) * H + h) * d;"),
     ("causal_excludes_diagonal", "if (causal && pos + 1 < z) z = pos + 1;",
@@ -50,6 +51,13 @@ MUTANTS = [
     ("fp16_subnormal_wrong", "ldexp((double)mant, -24)", "ldexp((double)mant, -25)"),
     ("bf16_shift_wrong", "(uint32_t)bits << 16", "(uint32_t)bits << 15"),
     ("lse_stride_wrong", "lse + (b * H + h) * Nq + i", "lse + (b * H + h) * Nq + 0"),
+    ("bwd_drops_D", "dS[i * N + j] = P[i * N + j] * (dS[i * N + j] - Di);",
+     "dS[i * N + j] = P[i * N + j] * dS[i * N + j];"),
+    ("bwd_dq_unscaled", "for (int64_t c = 0; c < d; ++c) out[c] *= scale;", ""),
+    ("bwd_dv_from_dS", "const double ds = dS[i * N + j], p = P[i * N + j];",
+     "const double ds = dS[i * N + j], p = dS[i * N + j];"),
+    ("bwd_dk_transposed", "const double ds = dS[i * N + j], p = P[i * N + j];",
+     "const double ds = dS[j * N + i], p = P[i * N + j];"),
 ]
 
 
