@@ -133,9 +133,9 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 /* Bytes of workspace fa_fwd_splitkv needs: B*H*Nq*num_splits*(d + 1)*4; 0 for one part. */
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int d, int num_splits);
 
-/* A part count for fa_fwd_splitkv: 1 when the (b, h, Q block) units alone give every one of
- * num_sms SMs a CTA; otherwise enough parts to do so, each keeping at least 4 K/V tiles of
- * 128 keys, at most 128. */
+/* A part count for fa_fwd_splitkv on a GPU with num_sms SMs: the count (1..128, each part
+ * keeping at least 2 K/V tiles of 128 keys) that minimises waves of CTAs x (K/V tiles per part
+ * + 4), a model of one CTA per SM streaming its tiles after a fixed start-up cost. */
 int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int num_sms);
 
 /*

@@ -209,11 +209,20 @@ int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int num_sms) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || num_sms < 1) return 1;
   const long long units = (long long)B * H * ((Nq + 255) / 256);
   const long long kv_tiles = (Nk + 127) / 128;
-  if (units >= num_sms) return 1;
-  // Enough parts to give every SM a CTA, each part keeping at least 4 K/V tiles.
-  long long splits = (num_sms + units - 1) / units;
-  splits = std::min<long long>(splits, std::max<long long>(1, kv_tiles / 4));
-  return (int)std::max<long long>(1, std::min<long long>(splits, fa::MAX_SPLITS));
+  // Time model: waves of CTAs x (K/V tiles per part + a fixed cost of about 4 tiles per CTA
+  // for its prologue, epilogue and share of the merge). Parts keep at least 2 tiles.
+  const long long max_splits = std::max<long long>(1, std::min<long long>(fa::MAX_SPLITS,
+                                                                          kv_tiles / 2));
+  long long best = 1, best_cost = -1;
+  for (long long s = 1; s <= max_splits; ++s) {
+    const long long waves = (units * s + num_sms - 1) / num_sms;
+    const long long cost = waves * ((kv_tiles + s - 1) / s + 4);
+    if (best_cost < 0 || cost < best_cost) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  return (int)best;
 }
 
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -94,10 +94,12 @@ def test_splitkv_workspace_size_and_split_count(lib):
     assert lib.fa_fwd_splitkv_workspace_size(2, 3, 5, 128, 1) == 0
     # enough (b, h, Q block) units for every SM: no split
     assert lib.fa_fwd_splitkv_num_splits(2, 16, 8192, 8192, 152) == 1
-    # decoding, 4 x 8 heads, 64K keys: ceil(152 / 32) = 5 parts
-    assert lib.fa_fwd_splitkv_num_splits(4, 8, 1, 65536, 152) == 5
-    # few keys: at least 4 K/V tiles of 128 per part
-    assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 1024, 152) == 2
+    # decoding, 64K keys (512 tiles): waves x (tiles per part + 4) is smallest at 7 parts for
+    # 128 heads (6 waves x 78) and at 9 parts for 32 heads (2 waves x 61)
+    assert lib.fa_fwd_splitkv_num_splits(4, 32, 1, 65536, 152) == 7
+    assert lib.fa_fwd_splitkv_num_splits(4, 8, 1, 65536, 152) == 9
+    # few keys: parts keep at least 2 tiles
+    assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 1024, 152) == 4
     assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 100, 152) == 1
     assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 1 << 30, 152) == 128
 
