@@ -164,6 +164,34 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
                            int window_right, const int* seqlens_k, float scale, int dtype,
                            int num_splits, fa_stream_t stream);
 
+/*
+ * fa_bwd -- gradients of the forward: dQ, dK, dV of L = sum(dO * O) for O = fa_fwd(q, k, v).
+ * The forward keeps, per row, the softmax statistics the backward needs ("FlashAttention V2
+ * 核心原理与架构设计" §2.3 keeps m and l; here their combination LSE = m + ln l), so the
+ * backward rebuilds P_ij = exp(scale <q_i, k_j> - LSE_i) tile by tile without storing it:
+ *   dV = P^T dO,  dP = dO V^T,  dS = P (dP - D) with D_i = <dO_i, O_i>,
+ *   dQ = scale dS K,  dK = scale dS^T Q.
+ *
+ *   q, k, v, o   [B, N, H, d] dtype: the forward's inputs and output
+ *   dout         [B, N, H, d] dtype: the gradient of the loss with respect to o
+ *   lse          [B, H, N] fp32: the forward's LSE for the same q, k, v, causal and scale
+ *   dq, dk, dv   [B, N, H, d] dtype, written (every element)
+ *   causal, scale, dtype, d: as in fa_fwd (no window or key-length masks here)
+ *   workspace    device memory of at least fa_bwd_workspace_size(B, H, N, d) bytes, 16-byte
+ *                aligned, owned by the caller, not overlapping any other argument: fp32 dQ
+ *                partial sums and D. Calls sharing a workspace must not overlap.
+ * Returns as fa_fwd; on a host-detected error nothing is enqueued. Enqueues three kernels on
+ * `stream`: D and a cleared dQ accumulator, the main kernel (one CTA per (b, h, 128-key
+ * block)), and the rounding of dQ.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+           fa_stream_t stream);
+
+/* Bytes of workspace fa_bwd needs: B*H*N*(d + 1)*4. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
 /* Static English text for a status code (never NULL). */
 const char* fa_error_string(int code);
 

@@ -59,6 +59,11 @@ def load_library() -> ctypes.CDLL:
             lib.fa_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
             lib.fa_fwd_splitkv_num_splits.argtypes = [i32, i32, i32, i32, i32]
             lib.fa_fwd_splitkv_num_splits.restype = i32
+            lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                   f32, i32, vp, ctypes.c_size_t, vp]
+            lib.fa_bwd.restype = i32
+            lib.fa_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
+            lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
             lib.fa_error_string.argtypes = [i32]
             lib.fa_error_string.restype = ctypes.c_char_p
             lib.fa_get_device_error.argtypes = [vp]
@@ -200,6 +205,36 @@ def fa_fwd_splitkv(q, k, v, o, lse, causal: bool, scale: float, num_splits: int,
         ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_splitkv")
+
+
+def bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    """Bytes of workspace fa_bwd needs."""
+    return int(load_library().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool, scale: float, workspace=None,
+           stream=None) -> None:
+    """Enqueue the backward: dq, dk, dv [B, N, H, d] from the forward's q, k, v, o, lse and
+    the upstream gradient dout. ``workspace``: a CUDA tensor of at least bwd_workspace_size
+    bytes, or None to let PyTorch allocate one."""
+    import torch
+    B, N, H, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk),
+                    ("dv", dv)):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor like q" % name)
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be float32 [B, H, N]")
+    need = bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = load_library().fa_bwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+        _dtype_code(q), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
 
 
 def device_error(stream=None) -> int:

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(_ROOT, "include")
 BUILD_DIR = os.path.join(_PKG, "_build")
 LIB = os.path.join(BUILD_DIR, "libfa_gb300.so")
 
-SOURCES = ["fa_fwd_kernel.cu", "fa_api.cpp", "fa_noalloc.cu"]
+SOURCES = ["fa_fwd_kernel.cu", "fa_bwd_kernel.cu", "fa_api.cpp", "fa_noalloc.cu"]
 HEADERS = ["fa_internal.h", "ptx_sm103.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -234,11 +234,79 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 }
 
 int fa_get_device_error(fa_stream_t stream) {
-  int value = 0;
+  int value = 0, bwd_value = 0;
   if (fa::read_and_clear_device_error(reinterpret_cast<cudaStream_t>(stream), &value) !=
-      cudaSuccess)
+          cudaSuccess ||
+      fa::read_and_clear_bwd_error(&bwd_value) != cudaSuccess)
     return FA_ERR_CUDA;
-  return value == 0 ? FA_OK : FA_ERR_TIMEOUT;
+  return (value == 0 && bwd_value == 0) ? FA_OK : FA_ERR_TIMEOUT;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  const uint64_t rows = (uint64_t)B * (uint64_t)H * (uint64_t)N;
+  return (size_t)(rows * (uint64_t)d * 4 + rows * 4);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+           fa_stream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+    return FA_ERR_NULL;
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return FA_ERR_SHAPE;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
+  if (!isfinite(scale)) return FA_ERR_SCALE;
+  const uint64_t bh = (uint64_t)B * (uint64_t)H;
+  if (bh * (uint64_t)((N + 127) / 128) >= (1ull << 31)) return FA_ERR_SHAPE;
+  const uint64_t elems = bh * (uint64_t)N * (uint64_t)d;
+  if (elems > (1ull << 62) / 4) return FA_ERR_SHAPE;
+  if (workspace_bytes < fa_bwd_workspace_size(B, H, N, d)) return FA_ERR_WORKSPACE;
+  const uint64_t t_bytes = elems * 2, lse_bytes = bh * (uint64_t)N * 4;
+  for (const void* p : {q, k, v, o, dout, static_cast<const void*>(dq),
+                        static_cast<const void*>(dk), static_cast<const void*>(dv),
+                        static_cast<const void*>(workspace)})
+    if (reinterpret_cast<uintptr_t>(p) % 16) return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) % 4) return FA_ERR_ALIGN;
+  struct Span { const void* p; uint64_t n; };
+  const Span ins[] = {{q, t_bytes}, {k, t_bytes}, {v, t_bytes}, {o, t_bytes}, {dout, t_bytes},
+                      {lse, lse_bytes}};
+  const Span outs[] = {{dq, t_bytes}, {dk, t_bytes}, {dv, t_bytes},
+                       {workspace, fa_bwd_workspace_size(B, H, N, d)}};
+  for (const Span& out : outs)
+    for (const Span& in : ins)
+      if (overlaps(out.p, out.n, in.p, in.n)) return FA_ERR_ALIAS;
+  for (int i = 0; i < 4; ++i)
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return FA_ERR_ALIAS;
+
+  int device = 0;
+  int rc = check_arch(&device);
+  if (rc != FA_OK) return rc;
+  fa::BwdParams p;
+  const bool fp16 = dtype == FA_FP16;
+  if (!encode_bnhd(&p.tm_q, q, B, H, N, d, fp16) || !encode_bnhd(&p.tm_k, k, B, H, N, d, fp16) ||
+      !encode_bnhd(&p.tm_v, v, B, H, N, d, fp16) ||
+      !encode_bnhd(&p.tm_do, dout, B, H, N, d, fp16))
+    return FA_ERR_CUDA;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.dq_acc = static_cast<float*>(workspace);
+  p.dpre = static_cast<float*>(workspace) + elems;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.d = d;
+  p.causal = causal ? 1 : 0;
+  p.fp16 = fp16 ? 1 : 0;
+  p.scale = scale;
+  if (fa::launch_bwd(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  return FA_OK;
 }
 
 }  // extern "C"

@@ -49,4 +49,26 @@ long long fwd_num_ctas(int B, int H, int Nq, int num_splits);
 // Device error word of the current device: read (after synchronising `stream`) and clear.
 cudaError_t read_and_clear_device_error(cudaStream_t stream, int* value);
 
+struct BwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // [B, N, H, d] as in FwdParams
+  const void* o;        // [B, N, H, d] forward output
+  const void* dout;     // [B, N, H, d] upstream gradient
+  const float* lse;     // [B, H, N] from the forward
+  void* dq;             // [B, N, H, d]
+  void* dk;
+  void* dv;
+  float* dq_acc;        // workspace: fp32 [B, N, H, d]
+  float* dpre;          // workspace: fp32 [B, H, N], D = rowsum(dO * O)
+  int B, H, N, d;
+  int causal;
+  int fp16;
+  float scale;
+};
+
+// Enqueue the backward (pre-kernel, main kernel, post-kernel).
+cudaError_t launch_bwd(const BwdParams& p, cudaStream_t stream);
+size_t bwd_smem_bytes(int d);
+// The backward kernels' error word of the current device: read and clear (no synchronisation).
+cudaError_t read_and_clear_bwd_error(int* value);
+
 }  // namespace fa

@@ -192,10 +192,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // Instruction descriptor for kind::f16 (32 bit): D format f32 (1) in [4,6); A and B formats
 // in [7,10) and [10,13) (0 = f16, 1 = bf16); A / B major-ness in bits 15 / 16 (0 = K-major,
 // 1 = MN-major); N >> 3 in [17,23); M >> 4 in [24,29).
-__host__ __device__ constexpr uint32_t idesc_f16(bool fp16, int M, int N, bool b_mn_major) {
+__host__ __device__ constexpr uint32_t idesc_f16(bool fp16, int M, int N, bool b_mn_major,
+                                                 bool a_mn_major = false) {
   return (1u << 4) | ((fp16 ? 0u : 1u) << 7) | ((fp16 ? 0u : 1u) << 10) |
-         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Add four fp32 values to global memory (one vector reduction, no return value).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem], one CTA, 16-bit inputs, fp32 accumulate.

@@ -1,0 +1,76 @@
+"""Parity of the backward (fa_bwd) with the fp64 oracle's gradients.
+
+The GPU forward provides O and LSE (as a user would run it); the oracle differentiates the exact
+definition on the same bf16/fp16 inputs. Tolerances, derived from the arithmetic: P and dS are
+rounded to the input type before their products (2^-9 relative for bf16), D uses the rounded
+O, and the outputs are rounded to the input type, so each gradient is held to a relative L2
+error of 2e-2 and a largest element error of 5e-2 of its largest element.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import to_device
+from io_aware_attention_fa2_gb300.inputs import make_qkv, normal, round_to_bits, softmax_scale
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 2e-2
+REL_MAX = 5e-2
+
+
+def run_case(B, H, N, d, dtype, causal, seed):
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    qb, kb, vb = make_qkv(B, H, N, d, dtype, seed)
+    dob = round_to_bits(normal((B, N, H, d), seed + 9), dtype)
+    q, k, v, do = (to_device(x, dtype) for x in (qb, kb, vb, dob))
+    scale = softmax_scale(d)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device="cuda")
+    binding.fa_fwd(q, k, v, o, lse, causal, scale)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    binding.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, scale)
+    assert binding.device_error() == 0
+    got = [t.double().cpu().numpy() for t in (dq, dk, dv)]
+    ref = oracle.attention_bwd(qb, kb, vb, dob, causal, scale, dtype=dtype)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert np.isfinite(g).all(), name
+        err = np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)
+        mx = np.abs(g - r).max() / max(np.abs(r).max(), 1e-30)
+        assert err <= REL_L2 and mx <= REL_MAX, (name, B, H, N, d, dtype, causal, err, mx)
+
+
+@pytest.mark.parametrize("N", [1, 17, 128, 200, 257])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_shapes(N, d, causal):
+    run_case(2, 2, N, d, "bf16", causal, seed=900 + N + d)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_fp16(causal):
+    run_case(1, 3, 300, 128, "fp16", causal, seed=990)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_longer(causal):
+    run_case(1, 4, 1024, 128, "bf16", causal, seed=991)
+
+
+def test_bwd_bad_arguments():
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    q = torch.zeros(1, 128, 1, 64, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, 1, 128, device="cuda")
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.FaError) as e:
+        binding.fa_bwd(q, q, q, q, q, lse, torch.empty_like(q), torch.empty_like(q),
+                       torch.empty_like(q), False, 0.125, small)
+    assert e.value.code == -11
+    with pytest.raises(binding.FaError) as e:
+        binding.fa_bwd(q, q, q, q, q, lse, q, torch.empty_like(q), torch.empty_like(q), False,
+                       0.125)
+    assert e.value.code == -5
