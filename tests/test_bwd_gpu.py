@@ -4,7 +4,8 @@ The GPU forward provides O and LSE (as a user would run it); the oracle differen
 definition on the same bf16/fp16 inputs. Tolerances, derived from the arithmetic: P and dS are
 rounded to the input type before their products (2^-9 relative for bf16), D uses the rounded
 O, and the outputs are rounded to the input type, so each gradient is held to a relative L2
-error of 2e-2 and a largest element error of 5e-2 of its largest element.
+error of 2e-2 and a largest element error of 5e-2 of its largest element. Where the exact
+gradient vanishes (dQ and dK with a single key), the computed one must stay below 1e-3.
 """
 import numpy as np
 import pytest
@@ -37,8 +38,12 @@ def run_case(B, H, N, d, dtype, causal, seed):
     ref = oracle.attention_bwd(qb, kb, vb, dob, causal, scale, dtype=dtype)
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         assert np.isfinite(g).all(), name
-        err = np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)
-        mx = np.abs(g - r).max() / max(np.abs(r).max(), 1e-30)
+        if np.abs(r).max() < 1e-6:
+            # the exact gradient vanishes (e.g. dQ, dK with one key): only rounding is left
+            assert np.abs(g).max() <= 1e-3, (name, float(np.abs(g).max()))
+            continue
+        err = np.linalg.norm(g - r) / np.linalg.norm(r)
+        mx = np.abs(g - r).max() / np.abs(r).max()
         assert err <= REL_L2 and mx <= REL_MAX, (name, B, H, N, d, dtype, causal, err, mx)
 
 
