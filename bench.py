@@ -351,6 +351,23 @@ def run_gpu(args, w):
     def step():
         call()
 
+    bwd = args.pass_ == "bwd"
+    if bwd:
+        # O and LSE from the forward (outside the timed region), a seeded upstream gradient,
+        # one workspace: each timed step is one fa_bwd call (three kernels).
+        from io_aware_attention_fa2_gb300.inputs import normal, round_to_bits
+        call()
+        dob = round_to_bits(normal(qb.shape, w.seed + 9), w.dtype)
+        host.append(torch.from_numpy(dob.view(np.int16)).view(tdt).pin_memory())
+        dout = host[-1].to(dev)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        bwd_ws = torch.empty(binding.bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                             device=dev)
+
+        def step():
+            binding.fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, w.causal, w.scale, bwd_ws,
+                           stream)
+
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -383,8 +400,16 @@ def run_gpu(args, w):
     l_host = torch.empty((w.B, w.H, w.N), dtype=torch.float32, pin_memory=True)
 
     def e2e_step():
-        binding.attention_forward(*host, causal=w.causal, scale=w.scale, out=o_host,
+        binding.attention_forward(*host[:3], causal=w.causal, scale=w.scale, out=o_host,
                                   lse=l_host, stream=stream, device=dev)
+
+    if bwd:
+        o_pin = o.cpu().pin_memory()
+        l_pin = lse.cpu().pin_memory()
+
+        def e2e_step():
+            binding.attention_backward(*host[:3], o_pin, host[3], l_pin, causal=w.causal,
+                                       scale=w.scale, stream=stream, device=dev)
 
     for _ in range(max(1, args.warmup // 2)):
         e2e_step()
@@ -397,7 +422,7 @@ def run_gpu(args, w):
     torch.cuda.synchronize(dev)
     e2e_ms = 1e3 * (time.perf_counter() - t0) / args.steps
 
-    flops = metric_flops(w)
+    flops = metric_flops(w) * (2.5 if bwd else 1.0)
     stats = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(stats, op=dist.ReduceOp.MAX)
@@ -410,8 +435,9 @@ def run_gpu(args, w):
         peak, peak_sus, hbm_peak, peak_src = measured_peaks()
         achieved = flops / (kernel_ms * 1e-3) / 1e12
         line = {
-            "metric": "attn fwd TFLOP/s (causal N=8K d=128 headline)" if w.name ==
-            DEFAULT_WORKLOAD else "attn fwd TFLOP/s",
+            "metric": ("attn bwd TFLOP/s (2.5x the forward's FLOPs)" if bwd else
+                       "attn fwd TFLOP/s (causal N=8K d=128 headline)" if w.name ==
+                       DEFAULT_WORKLOAD else "attn fwd TFLOP/s"),
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
@@ -424,7 +450,7 @@ def run_gpu(args, w):
             "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak,
                           "unit": "TFLOP/s", "frac": achieved / peak,
                           "peak_source": "%s (burst)" % peak_src,
-                          "traffic": traffic_record(w.name),
+                          "traffic": None if bwd else traffic_record(w.name),
                           "algorithmic_bytes": algorithmic_bytes(w)}
                          if not memory_bound(w) else
                          {"bound": "hbm",
@@ -435,12 +461,15 @@ def run_gpu(args, w):
                           "traffic": traffic_record(w.name),
                           "algorithmic_bytes": algorithmic_bytes(w)}),
             "num_splits": num_splits,
-            "gpu_launches_per_step": 2 if num_splits > 1 else 1,
+            "gpu_launches_per_step": 3 if bwd else 2 if num_splits > 1 else 1,
+            "pass": "bwd" if bwd else "fwd",
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host),
-                    "d2h_bytes_per_step": o_host.numel() * 2 + l_host.numel() * 4,
+                    "h2d_bytes_per_step": (sum(t.numel() * t.element_size() for t in host) +
+                                           ((o.numel() * 2 + lse.numel() * 4) if bwd else 0)),
+                    "d2h_bytes_per_step": (3 * o.numel() * 2 if bwd else
+                                           o_host.numel() * 2 + l_host.numel() * 4),
                     "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps * (2 if num_splits > 1 else 1),
+            "gpu_launches": args.steps * (3 if bwd else 2 if num_splits > 1 else 1),
             "kernel_ms": {"mean": kernel_ms, "min": min(per_step_ms),
                           "max": max(per_step_ms)},
             "wall_s_timed_region": t_wall,
@@ -465,7 +494,7 @@ def run_gpu(args, w):
                 og = o_std[idx[0], idx[2], idx[1]].double().cpu().numpy()
                 std["parity_max_abs_o"] = float(np.abs(og - o_ref).max())
             line["standard_attention"] = std
-        if not args.no_cpu_baseline and world == 1:
+        if not args.no_cpu_baseline and world == 1 and not bwd:
             line["cpu_baseline"] = {k: v for k, v in
                                     cpu_baseline(w, qb, kb, vb, args.cpu_seconds).items()}
         print(json.dumps(line), flush=True)
@@ -482,6 +511,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-check", action="store_true", help="skip the sampled parity check")
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
+                    help="time the forward (default) or the backward (dQ, dK, dV)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--vs-standard", action="store_true",
                     help="also time standard (materialised S, P) attention in PyTorch")

@@ -8,10 +8,11 @@ per-row fp32 log-sum-exp. The computation runs in hand-written CUDA kernels behi
 Importing the package does not load the CUDA library; the first call does, and raises if the
 library has not been built (there is no fallback path).
 """
-from .binding import (FaError, attention_forward, available, bwd_workspace_size,
+from .binding import (FaError, attention_backward, attention_forward, available,
+                      bwd_workspace_size,
                       device_error, error_string, fa_bwd, fa_fwd, fa_fwd_splitkv, library_path,
                       load_library, splitkv_num_splits, splitkv_workspace_size)
 
-__all__ = ["FaError", "attention_forward", "available", "bwd_workspace_size", "device_error",
+__all__ = ["FaError", "attention_backward", "attention_forward", "available", "bwd_workspace_size", "device_error",
            "error_string", "fa_bwd", "fa_fwd", "fa_fwd_splitkv", "library_path", "load_library", "splitkv_num_splits",
            "splitkv_workspace_size"]

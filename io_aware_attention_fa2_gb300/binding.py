@@ -294,3 +294,33 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         l_host.copy_(ld, non_blocking=True)
     st.synchronize()
     return o_host, l_host
+
+
+def attention_backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+                       stream=None, device=None):
+    """dq, dk, dv = gradients of sum(dout * o) for o, lse = attention_forward(q, k, v, causal).
+
+    Device tensors are used in place; host tensors (ideally pinned) are copied to ``device``
+    (default cuda:0), the kernels run there, and the gradients come back as host tensors.
+    """
+    import math
+
+    import torch
+    B, N, H, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+    if q.is_cuda:
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal, scale, None, stream)
+        return dq, dk, dv
+    dev = torch.device(device or "cuda:0")
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.stream(st):
+        dev_in = [t.to(dev, non_blocking=True) for t in (q, k, v, o, dout, lse)]
+        grads = [torch.empty_like(dev_in[0]) for _ in range(3)]
+        fa_bwd(*dev_in, *grads, causal, scale, None, st)
+        host = [torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned()) for _ in range(3)]
+        for h_, g_ in zip(host, grads):
+            h_.copy_(g_, non_blocking=True)
+    st.synchronize()
+    return tuple(host)
