@@ -10,25 +10,31 @@
 // Work split: one CTA per (b, h, K/V block j of 128 keys); K_j, V_j stay in shared memory and
 // dK_j, dV_j accumulate in TMEM while the CTA walks the Q blocks i that can see block j (all of
 // them, or i >= j when causal: the FA2 loop order with the roles of the two operands swapped).
-// Each step's dQ_i contribution is added to an fp32 workspace with vector reductions; a
-// pre-kernel computes D and clears the workspace, a post-kernel rounds dQ.
+// Each step's dQ_i contribution is added to an fp32 workspace laid out [B, H, N, d] (one Q
+// block's rows are one contiguous 128 x d block, which keeps the reductions' addresses
+// compact); a pre-kernel computes D and clears the workspace, a post-kernel scales, rounds and
+// transposes dQ back to [B, N, H, d].
 //
-// Per step (Q block i), all MMAs M = 128, fp32 accumulators in TMEM:
+// Per step (Q block i), all MMAs 128 x 128 x d or 128 x d x 128, fp32 accumulators in TMEM:
 //   S^T  = K_j Q_i^T     (smem x smem)            -> T_S   lanes = keys, columns = queries
 //   dP^T = V_j dO_i^T    (smem x smem)            -> T_dP
-//   compute warps: P^T = exp2(S^T scale log2e - LSE_i log2e) (masked), written back over T_S
-//                  as 16-bit pairs; dS'^T = scale P^T (dP^T - D_i), written over T_dP and, as
-//                  rows of dS'^T (queries contiguous), into shared memory
+//   softmax warps: P^T = exp2(S^T scale log2e - LSE_i log2e) (masked), written back over T_S
+//                  as 16-bit pairs; dS^T = P^T (dP^T - D_i) as rows (queries contiguous,
+//                  128-byte swizzle) into shared memory. The factor scale of dS' = scale dS is
+//                  applied to dK in its epilogue and to dQ when it is rounded.
 //   dV  += P^T dO_i      (TMEM x smem, dO MN-major)
-//   dK  += dS'^T Q_i     (TMEM x smem, Q MN-major)
-//   dQ_i = dS' K_j       (smem x smem: dS' M-major, K MN-major) -> T_dP, lanes = queries
-//   dQ warps: dQ_i rows -> fp32 workspace (red.global.add.v4.f32)
-// MMA issue order: dV(i), S^T(i+1), dK(i), dQ(i), dP^T(i+1): the next S^T runs while the
-// softmax warps compute dS'(i), and the next dP^T waits only for dQ(i) to be read out.
+//   dQ_i^T = K_j^T dS^T  (smem x smem, both MN-major; d = 128)  -> T_dP, lanes = features
+//   (d = 64: dQ_i = dS K_j, lanes = queries)
+//   dK  += dS^T Q_i      (smem x smem: the same dS rows read K-major, Q MN-major)
+//   dQ warps: dQ_i -> fp32 workspace (red.global.add: with lanes = features, one warp's
+//             reduction for a query is one 128-byte line)
+// MMA issue order: dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1): the next S^T runs while the
+// softmax warps compute dS(i); dQ(i)'s read-out overlaps dK(i), and the next dP^T waits only
+// for that read-out.
 // TMEM columns: T_S [0,128), T_dP [128,256), dV [256, 256+d), dK [256+d, 256+2d).
 //
 // Warps: 0 TMA producer (K_j, V_j once; Q_i, dO_i into a 2-deep ring), 1 MMA issuer and TMEM
-// allocator, 2..5 softmax / dS' (thread <-> TMEM lane), 6..9 dQ read-out and reduction.
+// allocator, 2..5 softmax / dS (thread <-> TMEM lane), 6..9 dQ read-out and reduction.
 // Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -73,8 +79,8 @@ enum : int {
   BB_S_FULL = BB_QD_EMPTY + kBwdStages,    // S^T computed
   BB_DP_FULL,                              // dP^T computed
   BB_P_FULL,                               // P^T in TMEM (128 arrivals)
-  BB_DS_FULL,                              // dS'^T in TMEM and shared memory (128 arrivals)
-  BB_DQ_FULL,                              // dQ_i in TMEM (T_dP; this step's dV, dK done)
+  BB_DS_FULL,                              // dS^T rows in shared memory (128 arrivals)
+  BB_DQ_FULL,                              // dQ_i (d = 128: dQ_i^T) in TMEM (T_dP)
   BB_DQ_TAKEN,                             // dQ_i read out of TMEM (128 arrivals)
   BB_STAT,                                 // this step's LSE, D in shared memory (128)
   BB_MMA_DONE,
@@ -142,18 +148,67 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// dQ (input type) from the fp32 workspace, element-wise.
-template <bool FP16>
+// dQ (input type) = scale x the fp32 workspace (which holds sum_j dS_ij k_j), element-wise.
+template <int D, bool FP16>
 __global__ void __launch_bounds__(256)
-    fa_bwd_post_kernel(const float* __restrict__ dq_acc, void* __restrict__ dq,
-                       long long pairs) {
+    fa_bwd_post_kernel(const float* __restrict__ dq_acc, void* __restrict__ dq, float scale,
+                       int H, int N, long long pairs) {
   const long long t = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
   if (t >= pairs) return;
-  const float2 v = reinterpret_cast<const float2*>(dq_acc)[t];
-  static_cast<uint32_t*>(dq)[t] = pack2<FP16>(v.x, v.y);
+  // t = pair of dq [B, N, H, d]; the workspace is [B, H, N, d]
+  const long long row = t / (D / 2), c2 = t % (D / 2);
+  const long long h = row % H, bq = row / H, q = bq % N, b = bq / N;
+  const float2 v = reinterpret_cast<const float2*>(dq_acc + ((b * H + h) * N + q) * D)[c2];
+  static_cast<uint32_t*>(dq)[t] = pack2<FP16>(v.x * scale, v.y * scale);
 }
 
 // ---------------------------------------------------------------------------------------------
+// P^T for 32 queries of this thread's key, packed to 16-bit pairs: 2^(S^T scale log2e -
+// LSE log2e). l2 holds the 32 queries' LSE log2e (+inf for rows to ignore). MASKED: the first
+// `lim` queries of the chunk do not see the key (causal diagonal, keys past N).
+template <bool MASKED, bool FP16>
+__device__ __forceinline__ void p_chunk(const uint32_t (&sr)[32], const float* __restrict__ l2,
+                                        float scale_log2, int lim, uint32_t* __restrict__ out) {
+#pragma unroll
+  for (int t4 = 0; t4 < 8; ++t4) {
+    const float4 l = reinterpret_cast<const float4*>(l2)[t4];
+    float x0, x1, x2, x3;
+    ptx::fma2(x0, x1, __uint_as_float(sr[4 * t4]), __uint_as_float(sr[4 * t4 + 1]), scale_log2,
+              scale_log2, -l.x, -l.y);
+    ptx::fma2(x2, x3, __uint_as_float(sr[4 * t4 + 2]), __uint_as_float(sr[4 * t4 + 3]),
+              scale_log2, scale_log2, -l.z, -l.w);
+    if constexpr (MASKED) {
+      if (4 * t4 < lim) x0 = -INFINITY;
+      if (4 * t4 + 1 < lim) x1 = -INFINITY;
+      if (4 * t4 + 2 < lim) x2 = -INFINITY;
+      if (4 * t4 + 3 < lim) x3 = -INFINITY;
+    }
+    out[2 * t4] = pack2<FP16>(ptx::exp2_approx(x0), ptx::exp2_approx(x1));
+    out[2 * t4 + 1] = pack2<FP16>(ptx::exp2_approx(x2), ptx::exp2_approx(x3));
+  }
+}
+
+// dS^T = P^T (dP^T - D) for 32 queries, packed to 16-bit pairs (scale is applied to dQ, dK).
+template <bool FP16>
+__device__ __forceinline__ void ds_chunk(const uint32_t (&dr)[32], const uint32_t* __restrict__ pp,
+                                         const float* __restrict__ dd, uint32_t (&out)[16]) {
+#pragma unroll
+  for (int t4 = 0; t4 < 8; ++t4) {
+    const float4 dv = reinterpret_cast<const float4*>(dd)[t4];
+    float p0, p1, p2, p3, e0, e1, e2, e3;
+    unpack2<FP16>(pp[2 * t4], p0, p1);
+    unpack2<FP16>(pp[2 * t4 + 1], p2, p3);
+    ptx::add2(e0, e1, __uint_as_float(dr[4 * t4]), __uint_as_float(dr[4 * t4 + 1]), -dv.x,
+              -dv.y);
+    ptx::add2(e2, e3, __uint_as_float(dr[4 * t4 + 2]), __uint_as_float(dr[4 * t4 + 3]), -dv.z,
+              -dv.w);
+    ptx::mul2(e0, e1, e0, e1, p0, p1);
+    ptx::mul2(e2, e3, e2, e3, p2, p3);
+    out[2 * t4] = pack2<FP16>(e0, e1);
+    out[2 * t4 + 1] = pack2<FP16>(e2, e3);
+  }
+}
+
 template <int D, bool FP16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -164,6 +219,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   void* __restrict__ dk_ptr, void* __restrict__ dv_ptr, int H, int N, int causal,
                   float scale, float scale_log2) {
   using L = BwdSmem<D>;
+  static_assert(L::kDynamic <= 227 * 1024, "backward tiles exceed shared memory");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
@@ -173,7 +229,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sK = smem_base + L::kK, sV = smem_base + L::kV;
   const uint32_t sQ = smem_base + L::kQ, sdO = smem_base + L::kdO, sdS = smem_base + L::kdS;
   float* const stat = reinterpret_cast<float*>(smem_gen + L::kStat);   // [2][128]
-  static_assert(BwdSmem<D>::kDynamic <= 227 * 1024, "backward tiles exceed shared memory");
   auto bar = [&](int i) { return smem_base + L::kBars + 8u * static_cast<uint32_t>(i); };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -181,10 +236,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int num_kv = (N + BLOCK_N - 1) / BLOCK_N;
   const int num_q = (N + BLOCK_M - 1) / BLOCK_M;
   const int bh = static_cast<int>(blockIdx.x) / num_kv;
-  const int rj = static_cast<int>(blockIdx.x) % num_kv;
-  const int jb = rj;                                     // K/V block (block 0 sees most Q)
+  const int jb = static_cast<int>(blockIdx.x) % num_kv;   // K/V block (block 0 sees most Q)
   const int b = bh / H, h = bh % H;
-  const int i0 = causal ? jb : 0;                        // first Q block that sees block jb
+  const int i0 = causal ? jb : 0;                          // first Q block that sees block jb
   const int steps = num_q - i0;
 
   if (threadIdx.x == 0) {
@@ -255,9 +309,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_st = ptx::idesc_f16(FP16, 128, BLOCK_M, false);         // S^T, dP^T
-      constexpr uint32_t id_acc = ptx::idesc_f16(FP16, 128, D, true);               // dV, dK
-      constexpr uint32_t id_dq = ptx::idesc_f16(FP16, BLOCK_M, D, true, true);      // dQ
+      constexpr uint32_t id_st = ptx::idesc_f16(FP16, 128, BLOCK_M, false);   // S^T, dP^T
+      constexpr uint32_t id_acc = ptx::idesc_f16(FP16, 128, D, true);         // dV, dK
+      // d = 128: dQ^T = K_j^T dS'^T (M = features); d = 64: dQ = dS' K_j (M = queries).
+      constexpr uint32_t id_dq = D == 128 ? ptx::idesc_f16(FP16, D, BLOCK_M, true, true)
+                                          : ptx::idesc_f16(FP16, BLOCK_M, D, true, true);
       auto qbase = [&](int n) { return sQ + (n % kBwdStages) * L::kTile; };
       auto dobase = [&](int n) { return sdO + (n % kBwdStages) * L::kTile; };
       // S^T = K_j Q_i^T -> T_S and dP^T = V_j dO_i^T -> T_dP: both operands K-major over d.
@@ -306,25 +362,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           issue_s(n + 1);
         }
-        // dK += dS'^T Q_i, same shapes with Q_i as B.
         if (!wait(BB_DS_FULL, n & 1)) { ok = false; break; }
         ptx::tc_fence_after_sync();
+        // dQ first, into T_dP (dP^T(i) is in the softmax threads' registers by now), so that
+        // its read-out overlaps dK. Both operands MN-major, 16 keys = 16 rows of 128 bytes per
+        // MMA: the dS' rows (queries contiguous) and K_j (d contiguous).
+#pragma unroll
+        for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
+          const uint64_t ds_desc = ptx::smem_desc_sw128(sdS + kk * 16 * 128, kBoxBytes, 1024);
+          const uint64_t k_desc = ptx::smem_desc_sw128(sK + kk * 16 * 128, kBoxBytes, 1024);
+          if constexpr (D == 128)
+            ptx::mma_f16_ss(tmem + kT_dP, k_desc, ds_desc, id_dq, kk > 0);
+          else
+            ptx::mma_f16_ss(tmem + kT_dP, ds_desc, k_desc, id_dq, kk > 0);
+        }
+        ptx::mma_commit(bar(BB_DQ_FULL));
+        // dK += dS'^T Q_i: A = the same dS' rows read K-major (queries are the K dimension),
+        // B = Q_i MN-major.
 #pragma unroll
         for (int kk = 0; kk < BLOCK_M / 16; ++kk)
-          ptx::mma_f16_ts(tmem + kT_dV + D, tmem + kT_dP + kk * 8,
+          ptx::mma_f16_ss(tmem + kT_dV + D,
+                          ptx::smem_desc_sw128(sdS + (kk / 4) * kBoxBytes + (kk % 4) * 32, 16,
+                                               1024),
                           ptx::smem_desc_sw128(qbase(n) + kk * 16 * 128, kBoxBytes, 1024),
                           id_acc, (n > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar(BB_QD_EMPTY + s));   // Q_i and dO_i are no longer read
-        // dQ_i = dS' K_j -> T_dP (after dK has read dS'^T there): A = dS' (queries contiguous,
-        // M-major) from shared memory, B = K_j (d contiguous, MN-major); 16 keys = 16 rows of
-        // 128 bytes per MMA for both.
-#pragma unroll
-        for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-          ptx::mma_f16_ss(tmem + kT_dP,
-                          ptx::smem_desc_sw128(sdS + kk * 16 * 128, kBoxBytes, 1024),
-                          ptx::smem_desc_sw128(sK + kk * 16 * 128, kBoxBytes, 1024), id_dq,
-                          kk > 0);
-        ptx::mma_commit(bar(BB_DQ_FULL));
         // dP^T(i+1) over dQ(i) once the dQ warps have read it out.
         if (next) {
           if (!wait(BB_DQ_TAKEN, n & 1)) { ok = false; break; }
@@ -336,169 +398,191 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       wait(BB_MMA_DONE, 0);
     }
     __syncwarp();
-  } else {
-    const int quarter = warp & 3;                 // TMEM lanes [32q, 32q+32)
-    const int r = quarter * 32 + lane;            // TMEM lane
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- softmax / dS' warps
+    // TMEM lane r = key jb * 128 + r for S^T, dP^T, dV, dK.
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int key = jb * BLOCK_N + r;
+    const bool key_ok = key < N;
+    uint8_t* const ds_gen = smem_gen + L::kdS;
+    float* const s_lse = stat;         // LSE_i * log2e, +inf for rows to ignore
+    float* const s_d = stat + 128;     // D_i
     bool ok = true;
-    if (warp < 6) {
-      // -------------------------------------------------------------- softmax / dS' warps
-      // lane r = key jb * 128 + r for S^T, dP^T, dV, dK
-      const int key = jb * BLOCK_N + r;
-      const bool key_ok = key < N;
-      uint8_t* const ds_gen = smem_gen + L::kdS;
-      for (int n = 0; n < steps; ++n) {
-        const int q0 = (i0 + n) * BLOCK_M;
-        float* const s_lse = stat;         // LSE_i * log2e, +inf for rows to ignore
-        float* const s_d = stat + 128;     // D_i
-        {
-          // This step's row statistics, one query per thread. Queries past N (and rows with
-          // no allowed key, LSE = -inf) get +inf, so their P is 0. One buffer serves every
-          // step: it is overwritten only after all 128 threads have finished the previous
-          // step's dS' (DS_FULL), the last phase that reads it.
-          const int q = q0 + r;
-          float l2 = INFINITY, dd = 0.f;
-          if (q < N) {
-            const float lv = lse[static_cast<int64_t>(bh) * N + q];
-            if (lv != -INFINITY) l2 = lv * kLog2e;
-            dd = dpre[static_cast<int64_t>(bh) * N + q];
-          }
-          if (n > 0 && !wait(BB_DS_FULL, (n - 1) & 1)) { ok = false; break; }
-          s_lse[r] = l2;
-          s_d[r] = dd;
-          ptx::mbar_arrive(bar(BB_STAT));
-          if (!wait(BB_STAT, n & 1)) { ok = false; break; }
-        }
-        // --- P^T: this thread's key against the 128 queries of block i
-        if (!wait(BB_S_FULL, n & 1)) { ok = false; break; }
-        ptx::tc_fence_after_sync();
-      // P^T, kept packed as 16-bit pairs (the values the dV product uses, also used for dS'):
-        // query q0 + t sees this key only if key <= q0 + t (causal); keys past N do not exist.
-        const int lim = !key_ok ? BLOCK_M : (causal ? min(max(key - q0, 0), BLOCK_M) : 0);
-        uint32_t pp[BLOCK_M / 2];
-#pragma unroll
-        for (int c = 0; c < BLOCK_M / 32; ++c) {
-          uint32_t sr[32];
-          ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_S + c * 32, sr);
-          ptx::tmem_wait_ld();
-          ptx::reg_fence(sr);
-#pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const int a = 32 * c + 2 * t;
-            float p0 = ptx::exp2_approx(fmaf(__uint_as_float(sr[2 * t]), scale_log2, -s_lse[a]));
-            float p1 = ptx::exp2_approx(
-                fmaf(__uint_as_float(sr[2 * t + 1]), scale_log2, -s_lse[a + 1]));
-            if (a < lim) p0 = 0.f;
-            if (a + 1 < lim) p1 = 0.f;
-            pp[16 * c + t] = pack2<FP16>(p0, p1);
-          }
-          uint32_t pr[16];
-#pragma unroll
-          for (int t = 0; t < 16; ++t) pr[t] = pp[16 * c + t];
-          ptx::tmem_st_32x32b_x16(tmem + lane_off + kT_S + c * 16, pr);
-        }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before_sync();
-        ptx::mbar_arrive(bar(BB_P_FULL));
-
-        // --- dS'^T = scale P^T (dP^T - D) -> TMEM (over dP^T) and shared memory (rows of dS'^T).
-        // dP^T(i) was issued after dQ(i-1) completed, so shared dS' is free again.
-        if (!wait(BB_DP_FULL, n & 1)) { ok = false; break; }
-        ptx::tc_fence_after_sync();
-#pragma unroll
-        for (int c = 0; c < BLOCK_M / 32; ++c) {
-          uint32_t dr[32];
-          ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + c * 32, dr);
-          ptx::tmem_wait_ld();
-          ptx::reg_fence(dr);
-          uint32_t pk[16];
-#pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const int a = 32 * c + 2 * t;
-            float p0, p1;
-            unpack2<FP16>(pp[16 * c + t], p0, p1);
-            const float d0 = scale * p0 * (__uint_as_float(dr[2 * t]) - s_d[a]);
-            const float d1 = scale * p1 * (__uint_as_float(dr[2 * t + 1]) - s_d[a + 1]);
-            pk[t] = pack2<FP16>(d0, d1);
-          }
-          ptx::tmem_st_32x32b_x16(tmem + lane_off + kT_dP + c * 16, pk);
-          // queries 32c .. 32c+31 of key row r: 4 chunks of 16 bytes in box c / 2, swizzled
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int chunk = (c % 2) * 4 + u;        // 16-byte chunk within the 128-byte row
-            const uint32_t off = (c / 2) * kBoxBytes + r * 128 + ((chunk ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(ds_gen + off) =
-                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          }
-        }
-        ptx::tmem_wait_st();
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before_sync();
-        ptx::mbar_arrive(bar(BB_DS_FULL));
-
+    // Row statistics, one query per thread, fetched a step ahead. Queries past N (and rows
+    // with no allowed key, LSE = -inf) get +inf, so their P is 0.
+    float l2_next = INFINITY, d_next = 0.f;
+    auto fetch_stats = [&](int n) {
+      const int q = (i0 + n) * BLOCK_M + r;
+      l2_next = INFINITY;
+      d_next = 0.f;
+      if (q < N) {
+        const float lv = lse[static_cast<int64_t>(bh) * N + q];
+        if (lv != -INFINITY) l2_next = lv * kLog2e;
+        d_next = dpre[static_cast<int64_t>(bh) * N + q];
       }
-      if (ok) {
-        // dK, dV rows. The last dQ completion implies this CTA's MMAs are all complete.
-        if (!wait(BB_DQ_FULL, (steps - 1) & 1)) ok = false;
-      }
-      if (ok) {
-        ptx::tc_fence_after_sync();
-#pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
-          uint16_t* out = static_cast<uint16_t*>(which ? dk_ptr : dv_ptr) +
-                          ((static_cast<int64_t>(b) * N + key) * H + h) * D;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t gr[32];
-            ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dV + which * D + c * 32, gr);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence(gr);
-            if (key_ok) {
-              uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+    };
+    fetch_stats(0);
+    for (int n = 0; n < steps; ++n) {
+      const int q0 = (i0 + n) * BLOCK_M;
+      // One buffer serves every step: it is refilled only after all 128 threads have
+      // finished the previous step's dS' (DS_FULL), the last phase that reads it.
+      if (n > 0 && !wait(BB_DS_FULL, (n - 1) & 1)) { ok = false; break; }
+      s_lse[r] = l2_next;
+      s_d[r] = d_next;
+      ptx::mbar_arrive(bar(BB_STAT));
+      if (!wait(BB_STAT, n & 1)) { ok = false; break; }
+      if (n + 1 < steps) fetch_stats(n + 1);
+
+      // --- P^T: this thread's key against the 128 queries of block i, kept packed as 16-bit
+      // pairs (the values the dV product uses, also used for dS'). Query q0 + t sees the key
+      // only if key <= q0 + t (causal); keys past N do not exist.
+      if (!wait(BB_S_FULL, n & 1)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      const int lim = !key_ok ? BLOCK_M : (causal ? min(max(key - q0, 0), BLOCK_M) : 0);
+      uint32_t pp[BLOCK_M / 2];
 #pragma unroll
-              for (int t = 0; t < 4; ++t)
-                dst[t] = make_uint4(
-                    pack2<FP16>(__uint_as_float(gr[8 * t]), __uint_as_float(gr[8 * t + 1])),
-                    pack2<FP16>(__uint_as_float(gr[8 * t + 2]), __uint_as_float(gr[8 * t + 3])),
-                    pack2<FP16>(__uint_as_float(gr[8 * t + 4]), __uint_as_float(gr[8 * t + 5])),
-                    pack2<FP16>(__uint_as_float(gr[8 * t + 6]), __uint_as_float(gr[8 * t + 7])));
+      for (int c = 0; c < BLOCK_M / 32; ++c) {
+        uint32_t sr[32];
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_S + c * 32, sr);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(sr);
+        if (lim > 32 * c)
+          p_chunk<true, FP16>(sr, s_lse + 32 * c, scale_log2, lim - 32 * c, pp + 16 * c);
+        else
+          p_chunk<false, FP16>(sr, s_lse + 32 * c, scale_log2, 0, pp + 16 * c);
+        uint32_t pr[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) pr[t] = pp[16 * c + t];
+        ptx::tmem_st_32x32b_x16(tmem + lane_off + kT_S + c * 16, pr);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before_sync();
+      ptx::mbar_arrive(bar(BB_P_FULL));
+
+      // --- dS^T = P^T (dP^T - D) -> rows of dS^T (queries contiguous) in shared memory, which
+      // both the dQ and the dK products read. dP^T(i) was issued after dQ(i-1) and dK(i-1)
+      // completed, so the buffer is free again.
+      if (!wait(BB_DP_FULL, n & 1)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < BLOCK_M / 32; ++c) {
+        uint32_t dr[32];
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + c * 32, dr);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(dr);
+        uint32_t pk[16];
+        ds_chunk<FP16>(dr, pp + 16 * c, s_d + 32 * c, pk);
+        // queries 32c .. 32c+31 of key row r: 4 chunks of 16 bytes in box c / 2, swizzled
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = (c % 2) * 4 + u;        // 16-byte chunk within the 128-byte row
+          const uint32_t off = (c / 2) * kBoxBytes + r * 128 + ((chunk ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(ds_gen + off) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before_sync();
+      ptx::mbar_arrive(bar(BB_DS_FULL));
+    }
+    // dK (times scale), dV rows once every MMA of this CTA has completed.
+    if (ok && !wait(BB_MMA_DONE, 0)) ok = false;
+    if (ok) {
+      ptx::tc_fence_after_sync();
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        uint16_t* out = static_cast<uint16_t*>(which ? dk_ptr : dv_ptr) +
+                        ((static_cast<int64_t>(b) * N + key) * H + h) * D;
+        const float f = which ? scale : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t gr[32];
+          ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dV + which * D + c * 32, gr);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(gr);
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              float g[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) g[e] = __uint_as_float(gr[8 * t + e]) * f;
+              dst[t] = make_uint4(pack2<FP16>(g[0], g[1]), pack2<FP16>(g[2], g[3]),
+                                  pack2<FP16>(g[4], g[5]), pack2<FP16>(g[6], g[7]));
             }
           }
         }
-      } else {
-        record_timeout(abort_p);
       }
     } else {
-      // -------------------------------------------------------------- dQ warps
-      // lane r = query q0 + r of dQ_i (in T_dP); its row goes into the fp32 workspace.
-      for (int n = 0; n < steps; ++n) {
-        const int q0 = (i0 + n) * BLOCK_M;
-        if (!wait(BB_DQ_FULL, n & 1)) { ok = false; break; }
-        ptx::tc_fence_after_sync();
-        // 32 columns at a time: the reductions of one chunk overlap the next chunk's load;
-        // T_dP is released as soon as the last chunk is in registers.
-        const bool row_ok = q0 + r < N;
-        float* dst = dq_acc + ((static_cast<int64_t>(b) * N + q0 + r) * H + h) * D;
+      record_timeout(abort_p);
+    }
+  } else {
+    // ---------------------------------------------------------------- dQ warps
+    // The whole dQ block is loaded out of TMEM before T_dP is released, then reduced into the
+    // fp32 workspace. d = 128: TMEM lane = feature, column = query, so one warp's reduction
+    // for a query covers 32 consecutive features (one 128-byte line). d = 64: lane = query.
+    const int quarter = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    bool ok = true;
+    for (int n = 0; n < steps; ++n) {
+      const int q0 = (i0 + n) * BLOCK_M;
+      if (!wait(BB_DQ_FULL, n & 1)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      if constexpr (D == 128) {
+        uint32_t v0[32], v1[32], v2[32], v3[32];
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + 0, v0);
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + 32, v1);
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + 64, v2);
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + 96, v3);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(v0);
+        ptx::reg_fence(v1);
+        ptx::reg_fence(v2);
+        ptx::reg_fence(v3);
+        ptx::tc_fence_before_sync();
+        ptx::mbar_arrive(bar(BB_DQ_TAKEN));
+        const int nq = min(BLOCK_M, N - q0);
+        const int64_t stride = D;
+        float* const base =
+            dq_acc + (static_cast<int64_t>(bh) * N + q0) * D + quarter * 32 + lane;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t qr[32];
-          ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + c * 32, qr);
-          ptx::tmem_wait_ld();
-          ptx::reg_fence(qr);
-          if (c == D / 32 - 1) {
-            ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(bar(BB_DQ_TAKEN));
-          }
-          if (row_ok) {
+        for (int t = 0; t < 32; ++t)
+          if (t < nq) ptx::red_add_f32(base + t * stride, __uint_as_float(v0[t]));
 #pragma unroll
-            for (int t = 0; t < 32; t += 4)
-              ptx::red_add_v4(dst + c * 32 + t, __uint_as_float(qr[t]), __uint_as_float(qr[t + 1]),
-                              __uint_as_float(qr[t + 2]), __uint_as_float(qr[t + 3]));
-          }
+        for (int t = 0; t < 32; ++t)
+          if (32 + t < nq) ptx::red_add_f32(base + (32 + t) * stride, __uint_as_float(v1[t]));
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (64 + t < nq) ptx::red_add_f32(base + (64 + t) * stride, __uint_as_float(v2[t]));
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (96 + t < nq) ptx::red_add_f32(base + (96 + t) * stride, __uint_as_float(v3[t]));
+      } else {
+        uint32_t v0[32], v1[32];
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + 0, v0);
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + 32, v1);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(v0);
+        ptx::reg_fence(v1);
+        ptx::tc_fence_before_sync();
+        ptx::mbar_arrive(bar(BB_DQ_TAKEN));
+        const int r = quarter * 32 + lane;
+        if (q0 + r < N) {
+          float* dst = dq_acc + (static_cast<int64_t>(bh) * N + q0 + r) * D;
+#pragma unroll
+          for (int t = 0; t < 32; t += 4)
+            ptx::red_add_v4(dst + t, __uint_as_float(v0[t]), __uint_as_float(v0[t + 1]),
+                            __uint_as_float(v0[t + 2]), __uint_as_float(v0[t + 3]));
+#pragma unroll
+          for (int t = 0; t < 32; t += 4)
+            ptx::red_add_v4(dst + 32 + t, __uint_as_float(v1[t]), __uint_as_float(v1[t + 1]),
+                            __uint_as_float(v1[t + 2]), __uint_as_float(v1[t + 3]));
         }
       }
-      if (!ok) record_timeout(abort_p);
     }
+    if (!ok) record_timeout(abort_p);
   }
 
   // ------------------------------------------------------------------ teardown
@@ -528,8 +612,8 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const long long pairs = rows * D / 2;
-  fa_bwd_post_kernel<FP16><<<static_cast<unsigned>((pairs + 255) / 256), 256, 0, stream>>>(
-      p.dq_acc, p.dq, pairs);
+  fa_bwd_post_kernel<D, FP16><<<static_cast<unsigned>((pairs + 255) / 256), 256, 0, stream>>>(
+      p.dq_acc, p.dq, p.scale, p.H, p.N, pairs);
   return cudaGetLastError();
 }
 

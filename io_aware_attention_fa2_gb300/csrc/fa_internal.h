@@ -57,7 +57,7 @@ struct BwdParams {
   void* dq;             // [B, N, H, d]
   void* dk;
   void* dv;
-  float* dq_acc;        // workspace: fp32 [B, N, H, d]
+  float* dq_acc;        // workspace: fp32 [B, H, N, d], sum over key blocks of dS K
   float* dpre;          // workspace: fp32 [B, H, N], D = rowsum(dO * O)
   int B, H, N, d;
   int causal;
