@@ -41,9 +41,16 @@ from io_aware_attention_fa2_gb300.inputs import WORKLOADS, make_workload, sample
 DEFAULT_WORKLOAD = "n8k_d128_causal"
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ["io_aware_attention_fa2_gb300/csrc/fa_fwd_kernel.cu",
-                  "io_aware_attention_fa2_gb300/csrc/ptx_sm103.cuh",
-                  "io_aware_attention_fa2_gb300/csrc/fa_internal.h"]
+# The sources each pass's dominant kernel is built from: a committed DRAM-traffic record is
+# only reported while their hash is the one the record was taken on.
+KERNEL_SOURCES = {
+    "fwd": ["io_aware_attention_fa2_gb300/csrc/fa_fwd_kernel.cu",
+            "io_aware_attention_fa2_gb300/csrc/ptx_sm103.cuh",
+            "io_aware_attention_fa2_gb300/csrc/fa_internal.h"],
+    "bwd": ["io_aware_attention_fa2_gb300/csrc/fa_bwd_kernel.cu",
+            "io_aware_attention_fa2_gb300/csrc/ptx_sm103.cuh",
+            "io_aware_attention_fa2_gb300/csrc/fa_internal.h"],
+}
 
 
 def metric_flops(w) -> float:
@@ -68,9 +75,9 @@ def memory_bound(w) -> bool:
     return metric_flops(w) / algorithmic_bytes(w) < 275.0
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kind: str = "fwd") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -91,9 +98,10 @@ def measured_peaks():
         return FALLBACK_BF16_TFLOPS, 0.0, FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel."""
-    path = os.path.join(ROOT, "profiles", "fa_fwd_%s_dram.txt" % workload)
+def traffic_record(workload: str, kind: str = "fwd"):
+    """DRAM bytes per launch of the pass's dominant kernel from the committed ncu summary, if
+    taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "fa_%s_%s_dram.txt" % (kind, workload))
     try:
         rec = {}
         with open(path) as f:
@@ -101,7 +109,7 @@ def traffic_record(workload: str):
                 if "=" in line and not line.startswith("#"):
                     key, val = line.split("=", 1)
                     rec[key.strip()] = val.strip()
-        if rec.get("kernel_source_hash") != kernel_source_hash():
+        if rec.get("kernel_source_hash") != kernel_source_hash(kind):
             return None
         return int(float(rec["dram_bytes_per_launch"]))
     except (OSError, KeyError, ValueError):
@@ -450,7 +458,7 @@ def run_gpu(args, w):
             "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak,
                           "unit": "TFLOP/s", "frac": achieved / peak,
                           "peak_source": "%s (burst)" % peak_src,
-                          "traffic": None if bwd else traffic_record(w.name),
+                          "traffic": traffic_record(w.name, "bwd" if bwd else "fwd"),
                           "algorithmic_bytes": algorithmic_bytes(w)}
                          if not memory_bound(w) else
                          {"bound": "hbm",
