@@ -94,12 +94,6 @@ __device__ __forceinline__ void record_timeout(volatile int* abort_flag) {
 }
 
 template <bool FP16>
-__device__ __forceinline__ float load_elem(const void* p, int64_t i) {
-  if constexpr (FP16) return __half2float(static_cast<const __half*>(p)[i]);
-  else return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
-}
-
-template <bool FP16>
 __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
   if constexpr (FP16) {
     const __half2 h = *reinterpret_cast<const __half2*>(&w);
@@ -123,8 +117,18 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// Four consecutive 16-bit elements (8 bytes) as fp32.
+template <bool FP16>
+__device__ __forceinline__ float4 load4(const void* p, int64_t i) {
+  const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p) + i);
+  float4 f;
+  unpack2<FP16>(w.x, f.x, f.y);
+  unpack2<FP16>(w.y, f.z, f.w);
+  return f;
+}
+
 // D[b, h, q] = <dO[b, q, h, :], O[b, q, h, :]> and dQ workspace rows cleared. One warp per
-// (b, q, h) row of the [B, N, H, d] tensors.
+// (b, q, h) row of the [B, N, H, d] tensors, 4 elements per lane.
 template <int D, bool FP16>
 __global__ void __launch_bounds__(256)
     fa_bwd_pre_kernel(const void* __restrict__ o, const void* __restrict__ dout,
@@ -134,13 +138,14 @@ __global__ void __launch_bounds__(256)
   if (row >= rows) return;
   const int lane = threadIdx.x % 32;
   float acc = 0.f;
-#pragma unroll
-  for (int c = lane; c < D; c += 32)
-    acc = fmaf(load_elem<FP16>(o, row * D + c), load_elem<FP16>(dout, row * D + c), acc);
+  if (4 * lane < D) {
+    const float4 a = load4<FP16>(o, row * D + 4 * lane);
+    const float4 g = load4<FP16>(dout, row * D + 4 * lane);
+    acc = fmaf(a.x, g.x, fmaf(a.y, g.y, fmaf(a.z, g.z, a.w * g.w)));
+    reinterpret_cast<float4*>(dq_acc + row * D)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  float4* z = reinterpret_cast<float4*>(dq_acc + row * D);
-  for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (lane == 0) {
     const long long h = row % H, bq = row / H;   // row = (b * N + q) * H + h
     const long long q = bq % N, b = bq / N;
@@ -148,18 +153,21 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// dQ (input type) = scale x the fp32 workspace (which holds sum_j dS_ij k_j), element-wise.
+// dQ[b, q, h, :] (input type) = scale x the workspace row [b, h, q, :] (which holds
+// sum_j dS_qj k_j). One warp per (b, q, h) row, 4 elements per lane.
 template <int D, bool FP16>
 __global__ void __launch_bounds__(256)
     fa_bwd_post_kernel(const float* __restrict__ dq_acc, void* __restrict__ dq, float scale,
-                       int H, int N, long long pairs) {
-  const long long t = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
-  if (t >= pairs) return;
-  // t = pair of dq [B, N, H, d]; the workspace is [B, H, N, d]
-  const long long row = t / (D / 2), c2 = t % (D / 2);
-  const long long h = row % H, bq = row / H, q = bq % N, b = bq / N;
-  const float2 v = reinterpret_cast<const float2*>(dq_acc + ((b * H + h) * N + q) * D)[c2];
-  static_cast<uint32_t*>(dq)[t] = pack2<FP16>(v.x * scale, v.y * scale);
+                       int H, int N, long long rows) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
+  if (row >= rows) return;
+  const int lane = threadIdx.x % 32;
+  if (4 * lane >= D) return;
+  const long long h = row % H, bq = row / H;   // row = (b * N + q) * H + h
+  const long long q = bq % N, b = bq / N;
+  const float4 v = reinterpret_cast<const float4*>(dq_acc + ((b * H + h) * N + q) * D)[lane];
+  reinterpret_cast<uint2*>(static_cast<uint16_t*>(dq) + row * D)[lane] =
+      make_uint2(pack2<FP16>(v.x * scale, v.y * scale), pack2<FP16>(v.z * scale, v.w * scale));
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -611,9 +619,8 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
       p.scale, p.scale * kLog2e);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const long long pairs = rows * D / 2;
-  fa_bwd_post_kernel<D, FP16><<<static_cast<unsigned>((pairs + 255) / 256), 256, 0, stream>>>(
-      p.dq_acc, p.dq, p.scale, p.H, p.N, pairs);
+  fa_bwd_post_kernel<D, FP16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      p.dq_acc, p.dq, p.scale, p.H, p.N, rows);
   return cudaGetLastError();
 }
 
