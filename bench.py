@@ -175,6 +175,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values, world: int, device=None):
+    """Each timing (ms) replaced by its maximum over the ranks of the default process group
+    (the slowest rank sets the job's time); unchanged when world == 1."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_tflops(world: int, flops_per_rank_step: float, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: the FLOPs all ranks processed in `steps` steps over the slowest
+    rank's time for them (each rank runs its own replica of the workload)."""
+    return world * flops_per_rank_step * steps / (max_ms * 1e-3) / 1e12
+
+
 class OracleSampler:
     """Times the oracle on uniformly sampled query rows of a workload (bounded CPU work)."""
 
@@ -305,10 +322,10 @@ def run_gpu(args, w):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if rank == 0 or not os.path.exists(binding.library_path()):
+    if rank == 0:
         fa_build.build()
     if world > 1:
-        dist.barrier()
+        dist.barrier()   # the other ranks load what rank 0 built
     binding.load_library()
 
     qb, kb, vb = make_workload(w)
@@ -431,13 +448,10 @@ def run_gpu(args, w):
     e2e_ms = 1e3 * (time.perf_counter() - t0) / args.steps
 
     flops = metric_flops(w) * (2.5 if bwd else 1.0)
-    stats = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(stats, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = (float(x) for x in stats.cpu())
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    value = job_tflops(world, flops, args.steps, total_ms)
+    e2e_value = job_tflops(world, flops, 1, e2e_ms)
 
     if rank == 0:
         peak, peak_sus, hbm_peak, peak_src = measured_peaks()
