@@ -277,6 +277,25 @@ def run_reference(args, w):
     return 0
 
 
+# Standard attention's HBM accesses for one head, in the order "FlashAttention V2 核心原理与架构设计"
+# §1.1 lists them: Q and K read, S = QK^T written, S read, P = softmax(S) written, P and V read,
+# O = PV written.
+STANDARD_ATTENTION_HBM_ACCESSES = ("read Q", "read K", "write S", "read S", "write P", "read P",
+                                   "read V", "write O")
+
+
+def score_matrix_bytes(n: int, elem_bytes: int) -> int:
+    """Bytes of one N x N attention score (or probability) matrix."""
+    return n * n * elem_bytes
+
+
+def standard_attention_hbm_bytes(n: int, d: int, elem_bytes: int) -> int:
+    """HBM bytes of the accesses above for one head: the N x d operands once each, the N x N
+    matrices S and P each written and read once."""
+    sizes = {"Q": n * d, "K": n * d, "V": n * d, "O": n * d, "S": n * n, "P": n * n}
+    return sum(sizes[a.split()[1]] for a in STANDARD_ATTENTION_HBM_ACCESSES) * elem_bytes
+
+
 def time_standard_attention(q, k, v, w, steps, flush, stream):
     """The standard three-step attention (S = QK^T, P = softmax(S), O = PV, with S and P
     written to and read back from HBM), in PyTorch bf16/fp16 on the same device: the
@@ -506,7 +525,10 @@ def run_gpu(args, w):
             std = {"ms": std_ms, "tflops": flops / (std_ms * 1e-3) / 1e12,
                    "fused_speedup": std_ms / kernel_ms,
                    "what": "PyTorch matmul -> softmax -> matmul, S and P materialised in HBM, "
-                           "same dtype, same L2 flush and CUDA-event timing"}
+                           "same dtype, same L2 flush and CUDA-event timing",
+                   "materialised_bytes": 2 * w.B * w.H * score_matrix_bytes(w.N, 2),
+                   "hbm_bytes_model": w.B * w.H * standard_attention_hbm_bytes(w.N, w.d, 2),
+                   "fused_algorithmic_bytes": algorithmic_bytes(w)}
             if parity is not None:
                 import oracle
                 rows = sample_rows(w.B, w.H, w.N, 8, seed=w.seed + 5)
