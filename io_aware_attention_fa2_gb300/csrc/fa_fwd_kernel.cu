@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     for (int j = x0; j < x1; ++j) {
-      if (!ptx::wait_bounded(bar(BAR_S_FULL + x), (j - x0) & 1, abort_p, kWaitLimitNs)) {
+      if (!ptx::wait_bounded_warp(bar(BAR_S_FULL + x), (j - x0) & 1, abort_p, kWaitLimitNs)) {
         ok = false;
         break;
       }
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           lse_part[part_row] = -INFINITY;
         }
       }
-    } else if (ok && ptx::wait_bounded(bar(BAR_O_DONE + x), (x1 - x0 - 1) & 1, abort_p,
+    } else if (ok && ptx::wait_bounded_warp(bar(BAR_O_DONE + x), (x1 - x0 - 1) & 1, abort_p,
                                        kWaitLimitNs)) {
       ptx::tc_fence_after_sync();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;

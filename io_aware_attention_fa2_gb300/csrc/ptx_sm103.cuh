@@ -70,6 +70,16 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// wait_bounded for all 32 lanes of a warp, with one answer for the warp (false if any lane
+// gave up). Warps that go on to warp-collective instructions (tcgen05.ld/st, .sync.aligned)
+// use it, so that those are reached by every lane or by none, even when a wait ends right at
+// its limit.
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
+                                                  const volatile int* abort_flag,
+                                                  uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag, limit_ns));
+}
+
 // ---------------------------------------------------------------------------------------------
 // TMA: 4-D tiled tensor load into shared memory, completing on an mbarrier (transaction bytes).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
