@@ -412,6 +412,31 @@ def run_gpu(args, w):
             binding.fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, w.causal, w.scale, bwd_ws,
                            stream)
 
+        if rank == 0 and not args.no_check:
+            # parity of dQ, dK, dV on sampled positions of one head against the fp64 oracle
+            import oracle
+            step()
+            if binding.device_error(stream) != 0:
+                raise RuntimeError("kernel wait timed out")
+            b0, h0 = w.B - 1, w.H // 2
+            pos = np.unique(np.concatenate([
+                [0, 1, 127, 128, w.N // 2, w.N - 1],
+                np.random.default_rng(w.seed + 6).integers(0, w.N, 6)]))
+            sq, sk, sv = oracle.attention_bwd_sampled(qb, kb, vb, dob, w.causal, w.scale,
+                                                      [(b0, h0)], pos, pos, dtype=w.dtype)
+            sel = torch.from_numpy(pos).to(dev)
+            got = [t[b0, sel, h0].double().cpu().numpy() for t in (dq, dk, dv)]
+            parity = {"head": [int(b0), int(h0)], "positions": int(len(pos))}
+            bad = False
+            for name, g, r in zip(("dq", "dk", "dv"), got, (sq[0], sk[0], sv[0])):
+                rel = float(np.linalg.norm(g - r) / np.linalg.norm(r))
+                mx = float(np.abs(g - r).max() / np.abs(r).max())
+                parity["rel_l2_" + name], parity["rel_max_" + name] = rel, mx
+                bad |= not (rel <= 2e-2 and mx <= 5e-2)
+            if bad:
+                print(json.dumps({"error": "parity failed", "parity": parity}), flush=True)
+                return 3
+
     for _ in range(args.warmup):
         flush.zero_()
         step()

@@ -256,6 +256,118 @@ int oracle_attention_rows(const void* q, const void* k, const void* v, int kind,
                                     rows, nrows, o_rows, lse_rows);
 }
 
+/*
+ * The same backward on sampled outputs, for sizes where the N x N matrices of
+ * oracle_attention_bwd do not fit in memory. The formulas are those of oracle_attention_bwd,
+ * evaluated element by element. For each sampled head (b, h) = (heads[2t], heads[2t+1]):
+ *   1. for every query i: the row maximum m_i and sum l_i of the forward's softmax (two passes
+ *      over the allowed keys), and D_i = sum_j P_ij dP_ij with P_ij = exp(s_ij - m_i) / l_i,
+ *      s_ij = scale <q_i, k_j>, dP_ij = <dO_i, v_j>;
+ *   2. for each sampled key j: dV_j = sum_i P_ij dO_i and dK_j = scale sum_i dS_ij q_i with
+ *      dS_ij = P_ij (dP_ij - D_i), over the queries i that see key j;
+ *   3. for each sampled query i: dQ_i = scale sum_j dS_ij k_j over the keys it sees.
+ * Masks: causal or none (queries and keys share N). Outputs (fp64, row-major):
+ * dq [nheads][nqueries][d], dk and dv [nheads][nkeys][d].
+ */
+int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, const void* dout,
+                                 int kind, int64_t B, int64_t H, int64_t N, int64_t d,
+                                 int causal, double scale, const int64_t* heads, int64_t nheads,
+                                 const int64_t* keys, int64_t nkeys, const int64_t* queries,
+                                 int64_t nqueries, double* dq, double* dk, double* dv) {
+    int rc = check_args(q, k, v, kind, B, H, N, N, d);
+    if (rc) return rc;
+    if (!dout || !heads || nheads < 0 || nkeys < 0 || nqueries < 0) return -1;
+    if ((nkeys && (!keys || !dk || !dv)) || (nqueries && (!queries || !dq))) return -1;
+    for (int64_t t = 0; t < nheads; ++t)
+        if (heads[2 * t] < 0 || heads[2 * t] >= B || heads[2 * t + 1] < 0 ||
+            heads[2 * t + 1] >= H) return -2;
+    for (int64_t t = 0; t < nkeys; ++t) if (keys[t] < 0 || keys[t] >= N) return -2;
+    for (int64_t t = 0; t < nqueries; ++t) if (queries[t] < 0 || queries[t] >= N) return -2;
+    double* m = (double*)malloc((size_t)N * sizeof(double));
+    double* l = (double*)malloc((size_t)N * sizeof(double));
+    double* D = (double*)malloc((size_t)N * sizeof(double));
+    if (!m || !l || !D) {
+        free(m);
+        free(l);
+        free(D);
+        return -4;
+    }
+    for (int64_t t = 0; t < nheads; ++t) {
+        const int64_t b = heads[2 * t], h = heads[2 * t + 1];
+#define ROW(i) ((((b) * N + (i)) * H + (h)) * d)
+        /* 1. row statistics of every query of this head */
+#pragma omp parallel for schedule(dynamic, 16)
+        for (int64_t i = 0; i < N; ++i) {
+            const int64_t hi = causal ? i + 1 : N;
+            double mi = -INFINITY;
+            for (int64_t j = 0; j < hi; ++j) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c)
+                    dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
+                if (scale * dot > mi) mi = scale * dot;
+            }
+            double li = 0.0, di = 0.0;
+            for (int64_t j = 0; j < hi; ++j) {
+                double dot = 0.0, dp = 0.0;
+                for (int64_t c = 0; c < d; ++c) {
+                    dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
+                    dp += elem(dout, kind, ROW(i) + c) * elem(v, kind, ROW(j) + c);
+                }
+                const double e = exp(scale * dot - mi);
+                li += e;
+                di += e * dp;
+            }
+            m[i] = mi;
+            l[i] = li;
+            D[i] = di / li;
+        }
+        /* 2. dV_j, dK_j for the sampled keys */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t u = 0; u < nkeys; ++u) {
+            const int64_t j = keys[u];
+            double* gk = dk + (t * nkeys + u) * d;
+            double* gv = dv + (t * nkeys + u) * d;
+            for (int64_t c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
+            for (int64_t i = causal ? j : 0; i < N; ++i) {
+                double dot = 0.0, dp = 0.0;
+                for (int64_t c = 0; c < d; ++c) {
+                    dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
+                    dp += elem(dout, kind, ROW(i) + c) * elem(v, kind, ROW(j) + c);
+                }
+                const double p = exp(scale * dot - m[i]) / l[i];
+                const double ds = p * (dp - D[i]);
+                for (int64_t c = 0; c < d; ++c) {
+                    gv[c] += p * elem(dout, kind, ROW(i) + c);
+                    gk[c] += ds * elem(q, kind, ROW(i) + c);
+                }
+            }
+            for (int64_t c = 0; c < d; ++c) gk[c] *= scale;
+        }
+        /* 3. dQ_i for the sampled queries */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t u = 0; u < nqueries; ++u) {
+            const int64_t i = queries[u];
+            double* gq = dq + (t * nqueries + u) * d;
+            for (int64_t c = 0; c < d; ++c) gq[c] = 0.0;
+            for (int64_t j = 0; j < (causal ? i + 1 : N); ++j) {
+                double dot = 0.0, dp = 0.0;
+                for (int64_t c = 0; c < d; ++c) {
+                    dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
+                    dp += elem(dout, kind, ROW(i) + c) * elem(v, kind, ROW(j) + c);
+                }
+                const double ds = exp(scale * dot - m[i]) / l[i] * (dp - D[i]);
+                for (int64_t c = 0; c < d; ++c) gq[c] += ds * elem(k, kind, ROW(j) + c);
+            }
+            for (int64_t c = 0; c < d; ++c) gq[c] *= scale;
+        }
+#undef ROW
+    }
+    free(m);
+    free(l);
+    free(D);
+    return 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -12,7 +12,8 @@ import pytest
 
 import oracle
 from gpu_util import to_device
-from io_aware_attention_fa2_gb300.inputs import make_qkv, normal, round_to_bits, softmax_scale
+from io_aware_attention_fa2_gb300.inputs import (WORKLOADS, make_qkv, make_workload, normal,
+                                                 round_to_bits, softmax_scale)
 
 pytestmark = pytest.mark.gpu
 
@@ -79,3 +80,38 @@ def test_bwd_bad_arguments():
         binding.fa_bwd(q, q, q, q, q, lse, q, torch.empty_like(q), torch.empty_like(q), False,
                        0.125)
     assert e.value.code == -5
+
+
+@pytest.mark.parametrize("name,heads", [("n8k_d128_causal", [(0, 3), (1, 12)]),
+                                        ("n8k_d128", [(1, 7)])])
+def test_bwd_full_size_sampled(name, heads):
+    """The benchmarked shape (B=2, H=16, N=8192, d=128 bf16) with the bench's upstream gradient,
+    one fa_bwd call as the bench launches it; dQ, dK, dV compared on sampled positions (tile
+    edges, the middle, the last row and seeded ones) of the given heads against the sampled
+    fp64 oracle."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    w = WORKLOADS[name]
+    qb, kb, vb = make_workload(w)
+    dob = round_to_bits(normal(qb.shape, w.seed + 9), w.dtype)
+    q, k, v, do = (to_device(x, w.dtype) for x in (qb, kb, vb, dob))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, device="cuda")
+    binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    binding.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale)
+    assert binding.device_error() == 0
+    pos = np.unique(np.concatenate([[0, 1, 127, 128, 129, w.N // 2, w.N - 128, w.N - 1],
+                                    np.random.default_rng(w.seed + 17).integers(0, w.N, 8)]))
+    ref = oracle.attention_bwd_sampled(qb, kb, vb, dob, w.causal, w.scale, heads, pos, pos,
+                                       dtype=w.dtype)
+    sel = torch.from_numpy(pos).cuda()
+    for t, (b, h) in enumerate(heads):
+        for name_g, g_all, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            g = g_all[b, sel, h].double().cpu().numpy()
+            r = r[t]
+            assert np.isfinite(g).all(), name_g
+            err = np.linalg.norm(g - r) / np.linalg.norm(r)
+            mx = np.abs(g - r).max() / np.abs(r).max()
+            assert err <= REL_L2 and mx <= REL_MAX, (name, b, h, name_g, err, mx)

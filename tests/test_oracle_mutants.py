@@ -58,6 +58,9 @@ MUTANTS = [
      "const double ds = dS[i * N + j], p = dS[i * N + j];"),
     ("bwd_dk_transposed", "const double ds = dS[i * N + j], p = P[i * N + j];",
      "const double ds = dS[j * N + i], p = P[i * N + j];"),
+    ("bwd_sampled_drops_D", "const double ds = p * (dp - D[i]);", "const double ds = p * dp;"),
+    ("bwd_sampled_causal_off_by_one", "for (int64_t i = causal ? j : 0; i < N; ++i) {",
+     "for (int64_t i = causal ? j + 1 : 0; i < N; ++i) {"),
 ]
 
 
