@@ -53,9 +53,30 @@ KERNEL_SOURCES = {
 }
 
 
+def allowed_pairs(w) -> int:
+    """Exact number of (b, h, query, key) pairs the workload's masks allow: key j is visible
+    to the query at position p (= i + Nk - Nq) when j < len_b, j <= p (causal),
+    p - left <= j (left >= 0) and j <= p + right (right >= 0)."""
+    nq, nk = w.N, w.n_keys
+    pos = np.arange(nq, dtype=np.int64) + (nk - nq)
+    total = 0
+    for b in range(w.B):
+        hi = np.full(nq, w.seqlens_k[b] if w.seqlens_k else nk, dtype=np.int64)
+        if w.causal:
+            hi = np.minimum(hi, pos + 1)
+        if w.window[1] >= 0:
+            hi = np.minimum(hi, pos + w.window[1] + 1)
+        lo = np.maximum(0, pos - w.window[0]) if w.window[0] >= 0 else np.zeros(nq, np.int64)
+        total += int(np.maximum(hi - lo, 0).sum())
+    return total * w.H
+
+
 def metric_flops(w) -> float:
     """4*B*H*N^2*d (halved when causal) for Nq = Nk; with fewer queries than keys, 4*B*H*d per
-    visible (query, key) pair (causal: query i sees i + Nk - Nq + 1 keys)."""
+    visible (query, key) pair (causal: query i sees i + Nk - Nq + 1 keys); with a padding or
+    window mask, 4*d per allowed pair, counted exactly."""
+    if w.masked:
+        return 4.0 * w.d * allowed_pairs(w)
     if not w.Nk:
         f = 4.0 * w.B * w.H * w.N * w.N * w.d
         return f / 2 if w.causal else f
@@ -215,7 +236,8 @@ class OracleSampler:
         rows = self.pick(n_rows)
         t0 = time.perf_counter()
         self.oracle.attention_rows(self.qb, self.kb, self.vb, rows, w.causal, w.scale,
-                                   dtype=w.dtype, lib=self.lib)
+                                   dtype=w.dtype, lib=self.lib, window=w.window,
+                                   seqlens_k=list(w.seqlens_k) or None)
         dt = time.perf_counter() - t0
         return metric_flops(w) * (len(rows) / self.total_rows), dt, len(rows)
 
@@ -363,12 +385,17 @@ def run_gpu(args, w):
 
     # parity on sampled rows before timing (rank 0)
     parity = None
+    lens_host = (torch.tensor(w.seqlens_k, dtype=torch.int32).pin_memory() if w.seqlens_k
+                 else None)
+    lens_dev = lens_host.to(dev) if w.seqlens_k else None
+
     def call():
         if w.Nk:
             binding.fa_fwd_splitkv(q, k, v, o, lse, w.causal, w.scale, num_splits, workspace,
                                    stream)
         else:
-            binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+            binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream, window=w.window,
+                           seqlens_k=lens_dev)
 
     if rank == 0 and not args.no_check:
         import oracle
@@ -377,7 +404,8 @@ def run_gpu(args, w):
             raise RuntimeError("kernel wait timed out")
         rows = sample_rows(w.B, w.H, w.N, 8, seed=w.seed + 5)
         o_ref, l_ref = oracle.attention_rows(qb, kb, vb, rows, w.causal, w.scale,
-                                             dtype=w.dtype)
+                                             dtype=w.dtype, window=w.window,
+                                             seqlens_k=list(w.seqlens_k) or None)
         idx = [torch.from_numpy(rows[:, c]).to(dev) for c in range(3)]
         og = o[idx[0], idx[2], idx[1]].double().cpu().numpy()
         lg = lse[idx[0], idx[1], idx[2]].double().cpu().numpy()
@@ -470,7 +498,8 @@ def run_gpu(args, w):
 
     def e2e_step():
         binding.attention_forward(*host[:3], causal=w.causal, scale=w.scale, out=o_host,
-                                  lse=l_host, stream=stream, device=dev)
+                                  lse=l_host, stream=stream, device=dev, window=w.window,
+                                  seqlens_k=lens_host)
 
     if bwd:
         o_pin = o.cpu().pin_memory()
@@ -531,7 +560,8 @@ def run_gpu(args, w):
             "pass": "bwd" if bwd else "fwd",
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": (sum(t.numel() * t.element_size() for t in host) +
-                                           ((o.numel() * 2 + lse.numel() * 4) if bwd else 0)),
+                                           ((o.numel() * 2 + lse.numel() * 4) if bwd else
+                                            (4 * len(w.seqlens_k)))),
                     "d2h_bytes_per_step": (3 * o.numel() * 2 if bwd else
                                            o_host.numel() * 2 + l_host.numel() * 4),
                     "ms_per_step": e2e_ms},
@@ -544,7 +574,7 @@ def run_gpu(args, w):
         }
         if peak_sus and not memory_bound(w):
             line["roofline"]["frac_of_sustained"] = achieved / peak_sus
-        if args.vs_standard and not w.Nk:
+        if args.vs_standard and not w.Nk and not w.masked:
             std_ms, o_std = time_standard_attention(q, k, v, w, min(args.steps, 20), flush,
                                                     stream)
             std = {"ms": std_ms, "tflops": flops / (std_ms * 1e-3) / 1e12,
@@ -591,6 +621,8 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
+    if args.pass_ == "bwd" and (w.Nk or w.masked):
+        ap.error("the backward takes one length N and the causal mask only")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_gpu(args, w)

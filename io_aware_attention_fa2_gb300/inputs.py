@@ -42,6 +42,8 @@ class Workload:
     k_outlier_frac: float = 0.0
     k_outlier_scale: float = 1.0
     Nk: int = 0           # keys (and values); 0 means N. Queries are then the last N positions.
+    window: tuple = (-1, -1)   # sliding window (left, right); negative = unbounded
+    seqlens_k: tuple = ()      # per-batch key lengths (padding mask); empty = all keys
 
     @property
     def scale(self) -> float:
@@ -51,11 +53,20 @@ class Workload:
     def n_keys(self) -> int:
         return self.Nk or self.N
 
+    @property
+    def masked(self) -> bool:
+        """A padding or sliding-window mask besides (or instead of) the causal one."""
+        return self.window != (-1, -1) or bool(self.seqlens_k)
+
     def describe(self) -> str:
         extra = ""
         if self.q_scale != 1.0 or self.k_outlier_frac:
             extra = ", Q x%g, %g%% of K rows x%g" % (self.q_scale, 100 * self.k_outlier_frac,
                                                       self.k_outlier_scale)
+        if self.window != (-1, -1):
+            extra += ", window (left, right) = (%d, %d)" % self.window
+        if self.seqlens_k:
+            extra += ", key lengths %s" % (list(self.seqlens_k),)
         n = ("N=%d" % self.N) if not self.Nk else ("Nq=%d Nk=%d" % (self.N, self.Nk))
         return "B=%d H=%d %s d=%d %s %s%s" % (self.B, self.H, n, self.d, self.dtype,
                                               "causal" if self.causal else "non-causal", extra)
@@ -80,6 +91,12 @@ WORKLOADS = {
     # N > 32K): 1 query per (b, h) attends to 65536 cached keys.
     "decode_nk64k_d128": Workload("decode_nk64k_d128", 4, 32, 1, 128, "bf16", True, 8000,
                                   Nk=65536),
+    # The extra masks at the headline shape: a causal sliding window of 1024 keys (the query and
+    # the 1023 before it), and key padding with the second sequence 5000 keys long.
+    "n8k_d128_window1k": Workload("n8k_d128_window1k", 2, 16, 8192, 128, "bf16", True, 9000,
+                                  window=(1023, -1)),
+    "n8k_d128_padded": Workload("n8k_d128_padded", 2, 16, 8192, 128, "bf16", False, 10000,
+                                seqlens_k=(8192, 5000)),
 }
 
 

@@ -8,7 +8,8 @@ import pytest
 
 import oracle
 from gpu_util import MAX_ABS_LSE, MAX_ABS_O, REL_L2_O, to_device
-from io_aware_attention_fa2_gb300.inputs import make_qkv, sample_rows, softmax_scale
+from io_aware_attention_fa2_gb300.inputs import (WORKLOADS, make_qkv, make_workload,
+                                                 sample_rows, softmax_scale)
 
 pytestmark = pytest.mark.gpu
 
@@ -95,6 +96,35 @@ def test_long_window_sampled():
     idx = [torch.from_numpy(rows[:, c]).cuda() for c in range(3)]
     check(o[idx[0], idx[2], idx[1]].double().cpu().numpy(),
           lse[idx[0], idx[1], idx[2]].double().cpu().numpy(), o_ref, lse_ref, "window 1024")
+
+
+@pytest.mark.parametrize("name", ["n8k_d128_window1k", "n8k_d128_padded"])
+def test_masked_workload_sampled(name):
+    """The masked workloads the benchmark times (B=2, H=16, N=8192, d=128), full size, one call
+    as the bench makes it; sampled rows of every head against the fp64 oracle, plus rows past
+    the shorter key length (padding) and the window's edge (sliding window)."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    w = WORKLOADS[name]
+    qb, kb, vb = make_workload(w)
+    q, k, v = (to_device(x, w.dtype) for x in (qb, kb, vb))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((w.B, w.H, w.N), float("nan"), dtype=torch.float32, device=q.device)
+    lens = list(w.seqlens_k) or None
+    lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32, device=q.device)
+    binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale, None, w.window, lens_t)
+    assert binding.device_error() == 0
+    rows = sample_rows(w.B, w.H, w.N, 64, seed=w.seed + 7)
+    extra = [(b, h, i) for b in range(w.B) for h in (0, w.H - 1)
+             for i in (1022, 1023, 1024, 1025, 4999, 5000, 5001, w.N - 1)]
+    rows = np.concatenate([rows, np.array(extra, dtype=rows.dtype)])
+    o_ref, lse_ref = oracle.attention_rows(qb, kb, vb, rows, w.causal, w.scale, dtype=w.dtype,
+                                           window=w.window, seqlens_k=lens)
+    idx = [torch.from_numpy(rows[:, c]).cuda() for c in range(3)]
+    check(o[idx[0], idx[2], idx[1]].double().cpu().numpy(),
+          lse[idx[0], idx[1], idx[2]].double().cpu().numpy(), o_ref, lse_ref, name)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
 
 
 def test_masked_bad_arguments():
