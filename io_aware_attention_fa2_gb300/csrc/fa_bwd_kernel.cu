@@ -19,8 +19,8 @@
 //   S^T  = K_j Q_i^T     (smem x smem)            -> T_S   lanes = keys, columns = queries
 //   dP^T = V_j dO_i^T    (smem x smem)            -> T_dP
 //   softmax warps: P^T = exp2(S^T scale log2e - LSE_i log2e) (masked), written back over T_S
-//                  as 16-bit pairs; dS^T = P^T (dP^T - D_i) as rows (queries contiguous,
-//                  128-byte swizzle) into shared memory. The factor scale of dS' = scale dS is
+//                  as 16-bit pairs and read back from there for dS^T = P^T (dP^T - D_i),
+//                  stored as rows (queries contiguous, 128-byte swizzle) in shared memory. The factor scale of dS' = scale dS is
 //                  applied to dK in its epilogue and to dQ when it is rounded.
 //   dV  += P^T dO_i      (TMEM x smem, dO MN-major)
 //   dQ_i^T = K_j^T dS^T  (smem x smem, both MN-major; d = 128)  -> T_dP, lanes = features
@@ -28,9 +28,10 @@
 //   dK  += dS^T Q_i      (smem x smem: the same dS rows read K-major, Q MN-major)
 //   dQ warps: dQ_i -> fp32 workspace (red.global.add: with lanes = features, one warp's
 //             reduction for a query is one 128-byte line)
-// MMA issue order: dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1): the next S^T runs while the
-// softmax warps compute dS(i); dQ(i)'s read-out overlaps dK(i), and the next dP^T waits only
-// for that read-out.
+// MMA issue order: dV(i), then (after dS(i)) S^T(i+1), dQ(i), dK(i), then dP^T(i+1): keeping
+// P^T(i) in TMEM until dS(i) has read it lets the softmax phases run as rolled loops (about a
+// quarter of the code, no register copy of P^T); dQ(i)'s read-out overlaps dK(i), and the
+// next dP^T waits only for that read-out.
 // TMEM columns: T_S [0,128), T_dP [128,256), dV [256, 256+d), dK [256+d, 256+2d).
 //
 // Warps: 0 TMA producer (K_j, V_j once; Q_i, dO_i into a 2-deep ring), 1 MMA issuer and TMEM
@@ -369,7 +370,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ptx::mma_f16_ts(tmem + kT_dV, tmem + kT_S + kk * 8,
                           ptx::smem_desc_sw128(dobase(n) + kk * 16 * 128, kBoxBytes, 1024),
                           id_acc, (n > 0 || kk > 0) ? 1u : 0u);
-        // S^T(i+1) over P^T(i): issued after dV(i), which reads P^T first (in-order pipe).
+        if (!wait(BB_DS_FULL, n & 1)) { ok = false; break; }
+        // S^T(i+1) over P^T(i): the softmax warps have read P^T(i) back for dS(i), and dV(i),
+        // issued before, reads it first (in-order pipe).
         if (next) {
           if (!wait(BB_QD_FULL + (n + 1) % kBwdStages, ((n + 1) / kBwdStages) & 1)) {
             ok = false;
@@ -377,7 +380,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           issue_s(n + 1);
         }
-        if (!wait(BB_DS_FULL, n & 1)) { ok = false; break; }
         ptx::tc_fence_after_sync();
         // dQ first, into T_dP (dP^T(i) is in the softmax threads' registers by now), so that
         // its read-out overlaps dK. Both operands MN-major, 16 keys = 16 rows of 128 bytes per
@@ -456,20 +458,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!wait_w(BB_S_FULL, n & 1)) { ok = false; break; }
       ptx::tc_fence_after_sync();
       const int lim = !key_ok ? BLOCK_M : (causal ? min(max(key - q0, 0), BLOCK_M) : 0);
-      uint32_t pp[BLOCK_M / 2];
-#pragma unroll
+      // P^T stays in TMEM (over the first 64 columns of S^T) until dS(i) has read it back.
+#pragma unroll 1
       for (int c = 0; c < BLOCK_M / 32; ++c) {
         uint32_t sr[32];
         ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_S + c * 32, sr);
         ptx::tmem_wait_ld();
         ptx::reg_fence(sr);
-        if (lim > 32 * c)
-          p_chunk<true, FP16>(sr, s_lse + 32 * c, scale_log2, lim - 32 * c, pp + 16 * c);
-        else
-          p_chunk<false, FP16>(sr, s_lse + 32 * c, scale_log2, 0, pp + 16 * c);
         uint32_t pr[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) pr[t] = pp[16 * c + t];
+        if (lim > 32 * c)
+          p_chunk<true, FP16>(sr, s_lse + 32 * c, scale_log2, lim - 32 * c, pr);
+        else
+          p_chunk<false, FP16>(sr, s_lse + 32 * c, scale_log2, 0, pr);
         ptx::tmem_st_32x32b_x16(tmem + lane_off + kT_S + c * 16, pr);
       }
       ptx::tmem_wait_st();
@@ -481,14 +481,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // completed, so the buffer is free again.
       if (!wait_w(BB_DP_FULL, n & 1)) { ok = false; break; }
       ptx::tc_fence_after_sync();
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < BLOCK_M / 32; ++c) {
-        uint32_t dr[32];
+        uint32_t dr[32], pw[16];
         ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + c * 32, dr);
+        ptx::tmem_ld_32x32b_x16(tmem + lane_off + kT_S + c * 16, pw);
         ptx::tmem_wait_ld();
         ptx::reg_fence(dr);
+        ptx::reg_fence(pw);
         uint32_t pk[16];
-        ds_chunk<FP16>(dr, pp + 16 * c, s_d + 32 * c, pk);
+        ds_chunk<FP16>(dr, pw, s_d + 32 * c, pk);
         // queries 32c .. 32c+31 of key row r: 4 chunks of 16 bytes in box c / 2, swizzled
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
