@@ -165,6 +165,31 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
                            int num_splits, fa_stream_t stream);
 
 /*
+ * fa_fwd_host -- fa_fwd on host buffers: the inputs are copied to device buffers, the forward
+ * runs there, and O and LSE are copied back, in groups of heads so that the copies of one
+ * group overlap the computation of another (each group is packed into a compact problem in the
+ * device buffers and unpacked on the way back). (The pages have no counterpart; this is the
+ * end-to-end form of fa_fwd for data that lives in host memory.)
+ *
+ *   q_h, k_h, v_h  [B, N, H, d] dtype, host memory: inputs
+ *   o_h            [B, N, H, d] dtype, host memory: output
+ *   lse_h          [B, H, N] fp32, host memory: output
+ *   q_d, k_d, v_d, o_d, lse_d  device buffers of the same sizes, owned by the caller, the
+ *                  arguments of the fa_fwd calls made here (same alignment and aliasing rules);
+ *                  their previous contents are overwritten
+ *   B, H, N, d, causal, scale, dtype: as in fa_fwd
+ * Page-locked (pinned) host memory lets the copies run asynchronously; with pageable memory
+ * the call is still correct but the copies do not overlap. Work is enqueued on `stream` and on
+ * two copy streams the library keeps per device; `stream` reaches completion (O and LSE in host
+ * memory) after everything enqueued here, so synchronise `stream` before reading o_h, lse_h,
+ * and keep every buffer alive until then. Returns as fa_fwd; on a host-detected error nothing is
+ * enqueued. Calls from several threads are serialised while they enqueue.
+ */
+int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d, int B, int H, int N,
+                int d, int causal, float scale, int dtype, fa_stream_t stream);
+
+/*
  * fa_bwd -- gradients of the forward: dQ, dK, dV of L = sum(dO * O) for O = fa_fwd(q, k, v).
  * The forward keeps, per row, the softmax statistics the backward needs ("FlashAttention V2
  * 核心原理与架构设计" §2.3 keeps m and l; here their combination LSE = m + ln l), so the

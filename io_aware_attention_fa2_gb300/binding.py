@@ -62,6 +62,8 @@ def load_library() -> ctypes.CDLL:
             lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                    f32, i32, vp, ctypes.c_size_t, vp]
             lib.fa_bwd.restype = i32
+            lib.fa_fwd_host.argtypes = [vp] * 10 + [i32, i32, i32, i32, i32, f32, i32, vp]
+            lib.fa_fwd_host.restype = i32
             lib.fa_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
             lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
             lib.fa_error_string.argtypes = [i32]
@@ -280,16 +282,33 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         return o, ls
     dev = torch.device(device or "cuda:0")
     st = stream if stream is not None else torch.cuda.current_stream(dev)
+    o_host = out if out is not None else torch.empty(q.shape, dtype=q.dtype,
+                                                     pin_memory=q.is_pinned())
+    l_host = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32,
+                                                     pin_memory=q.is_pinned())
+    plain = (not split and seqlens_k is None and tuple(window) == (-1, -1)
+             and all(t.is_contiguous() for t in (q, k, v, o_host, l_host))
+             and q.dtype in (torch.bfloat16, torch.float16) and k.dtype == q.dtype
+             and v.dtype == q.dtype and o_host.dtype == q.dtype)
+    if plain:
+        # fa_fwd_host: the library copies batch by batch, overlapping copies and compute.
+        with torch.cuda.device(dev):
+            qd, kd, vd, od = (torch.empty(q.shape, dtype=q.dtype, device=dev) for _ in range(4))
+            ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        rc = load_library().fa_fwd_host(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o_host.data_ptr(), l_host.data_ptr(),
+            qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), ld.data_ptr(),
+            B, H, N, d, int(bool(causal)), float(scale), _dtype_code(q), st.cuda_stream)
+        if rc != 0:
+            raise FaError(rc, "fa_fwd_host")
+        st.synchronize()
+        return o_host, l_host
     with torch.cuda.stream(st):
         qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
         od = torch.empty_like(qd)
         ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         lens = None if seqlens_k is None else seqlens_k.to(dev, torch.int32, non_blocking=True)
         run(qd, kd, vd, od, ld, st, lens)
-        o_host = out if out is not None else torch.empty(q.shape, dtype=q.dtype,
-                                                         pin_memory=q.is_pinned())
-        l_host = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32,
-                                                         pin_memory=q.is_pinned())
         o_host.copy_(od, non_blocking=True)
         l_host.copy_(ld, non_blocking=True)
     st.synchronize()

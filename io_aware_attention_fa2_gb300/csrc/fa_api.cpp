@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -106,11 +107,10 @@ const char* fa_error_string(int code) {
 
 namespace {
 
-// Shared checks and launch of every forward entry point.
-int run_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                int Nq, int Nk, int d, int causal, int window_left, int window_right,
-                const int* seqlens_k, float scale, int dtype, int num_splits, void* workspace,
-                size_t workspace_bytes, fa_stream_t stream) {
+// Host-side checks shared by every forward entry point (nothing is enqueued).
+int check_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int H, int Nq, int Nk, int d, int dtype, float scale, const int* seqlens_k,
+                  int num_splits, void* workspace, size_t workspace_bytes) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (B < 1 || H < 1 || Nq < 1 || Nk < Nq || (d != 64 && d != 128)) return FA_ERR_SHAPE;
   if (num_splits < 1 || num_splits > fa::MAX_SPLITS) return FA_ERR_SHAPE;
@@ -150,10 +150,19 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
     for (int j = i + 1; j < 3; ++j)
       if (outs[i].p && outs[j].p && overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n))
         return FA_ERR_ALIAS;
-
   int device = 0;
-  int rc = check_arch(&device);
+  return check_arch(&device);
+}
+
+// Shared checks and launch of every forward entry point.
+int run_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Nq, int Nk, int d, int causal, int window_left, int window_right,
+                const int* seqlens_k, float scale, int dtype, int num_splits, void* workspace,
+                size_t workspace_bytes, fa_stream_t stream) {
+  const int rc = check_forward(q, k, v, o, lse, B, H, Nq, Nk, d, dtype, scale, seqlens_k,
+                               num_splits, workspace, workspace_bytes);
   if (rc != FA_OK) return rc;
+  const uint64_t bh = (uint64_t)B * (uint64_t)H;
 
   fa::FwdParams p;
   const bool fp16 = dtype == FA_FP16;
@@ -231,6 +240,114 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   return run_forward(q, k, v, o, lse, B, H, Nq, Nk, d, causal, window_left, window_right,
                      seqlens_k, scale, dtype, num_splits, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Per device: the two copy streams of fa_fwd_host and its events, created on first use and
+// kept for the life of the process. One mutex serialises the enqueueing of fa_fwd_host calls,
+// so that two callers never interleave their event records and waits.
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  std::vector<cudaEvent_t> events;
+};
+std::mutex g_host_mutex;
+HostPipe g_host_pipe[kMaxDevices];
+
+int host_pipe(int device, size_t events, HostPipe** out) {
+  HostPipe& hp = g_host_pipe[device];
+  if (!hp.in && cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (!hp.out && cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess)
+    return FA_ERR_CUDA;
+  while (hp.events.size() < events) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return FA_ERR_CUDA;
+    hp.events.push_back(e);
+  }
+  *out = &hp;
+  return FA_OK;
+}
+
+constexpr int kHostChunks = 4;   // up to 2 * kHostChunks chunks per call
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d, int B, int H, int N,
+                int d, int causal, float scale, int dtype, fa_stream_t stream) {
+  if (!q_h || !k_h || !v_h || !o_h || !lse_h) return FA_ERR_NULL;
+  int rc = check_forward(q_d, k_d, v_d, o_d, lse_d, B, H, N, N, d, dtype, scale, nullptr, 1,
+                         nullptr, 0);
+  if (rc != FA_OK) return rc;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
+  // Chunks: groups of heads across all batches, packed by pitched copies into a compact
+  // [B, N, heads, d] problem in the device buffers and unpacked the same way. As many groups as
+  // keep two waves of work units (b, h, 256-row Q block) per chunk, at most kHostChunks * 2.
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      sms < 1)
+    return FA_ERR_CUDA;
+  const long long units = (long long)B * H * ((N + 255) / 256);
+  const int chunks = (int)std::max<long long>(
+      1, std::min<long long>({(long long)H, 2ll * kHostChunks, units / (2ll * sms)}));
+  std::lock_guard<std::mutex> lock(g_host_mutex);
+  HostPipe* hp = nullptr;
+  rc = host_pipe(device, 2 + 2 * (size_t)chunks, &hp);
+  if (rc != FA_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaEvent_t* ev = hp->events.data();   // [0] start, [1] end, then in/kernel per chunk
+  // The copy streams start after the work already on `stream`.
+  if (cudaEventRecord(ev[0], s) != cudaSuccess || cudaStreamWaitEvent(hp->in, ev[0], 0) ||
+      cudaStreamWaitEvent(hp->out, ev[0], 0))
+    return FA_ERR_CUDA;
+  const uint64_t head_row = (uint64_t)d * 2;                // bytes of one (b, n, h) row
+  const uint64_t hpitch = (uint64_t)H * head_row, height = (uint64_t)B * N;
+  uint64_t packed = 0, packed_lse = 0;                      // bytes / floats placed so far
+  for (int c = 0; c < chunks; ++c) {
+    const int h0 = (int)((int64_t)H * c / chunks), h1 = (int)((int64_t)H * (c + 1) / chunks);
+    const int hc = h1 - h0;
+    const uint64_t width = (uint64_t)hc * head_row;
+    char* qd = static_cast<char*>(q_d) + packed;
+    char* kd = static_cast<char*>(k_d) + packed;
+    char* vd = static_cast<char*>(v_d) + packed;
+    char* od = static_cast<char*>(o_d) + packed;
+    float* ld = lse_d + packed_lse;
+    const uint64_t host_off = (uint64_t)h0 * head_row;      // row (b, n) = (0, 0), head h0
+    cudaEvent_t ev_in = ev[2 + 2 * c], ev_k = ev[3 + 2 * c];
+    for (int t = 0; t < 3; ++t) {
+      const char* src = static_cast<const char*>(t == 0 ? q_h : t == 1 ? k_h : v_h) + host_off;
+      char* dst = t == 0 ? qd : t == 1 ? kd : vd;
+      if (cudaMemcpy2DAsync(dst, width, src, hpitch, width, height, cudaMemcpyHostToDevice,
+                            hp->in) != cudaSuccess)
+        return FA_ERR_CUDA;
+    }
+    if (cudaEventRecord(ev_in, hp->in) != cudaSuccess || cudaStreamWaitEvent(s, ev_in, 0))
+      return FA_ERR_CUDA;
+    rc = run_forward(qd, kd, vd, od, ld, B, hc, N, N, d, causal, -1, -1, nullptr, scale, dtype,
+                     1, nullptr, 0, stream);
+    if (rc != FA_OK) return rc;
+    if (cudaEventRecord(ev_k, s) != cudaSuccess || cudaStreamWaitEvent(hp->out, ev_k, 0) ||
+        cudaMemcpy2DAsync(static_cast<char*>(o_h) + host_off, hpitch, od, width, width, height,
+                          cudaMemcpyDeviceToHost, hp->out) != cudaSuccess)
+      return FA_ERR_CUDA;
+    // LSE rows (b, h) of the chunk: hc * N floats per batch, at (b * H + h0) * N in lse_h
+    if (cudaMemcpy2DAsync(lse_h + (uint64_t)h0 * N, (uint64_t)H * N * 4, ld,
+                          (uint64_t)hc * N * 4, (uint64_t)hc * N * 4, (uint64_t)B,
+                          cudaMemcpyDeviceToHost, hp->out) != cudaSuccess)
+      return FA_ERR_CUDA;
+    packed += width * height;
+    packed_lse += (uint64_t)B * hc * N;
+  }
+  // `stream` reaches this point once the last output copy is done.
+  if (cudaEventRecord(ev[1], hp->out) != cudaSuccess || cudaStreamWaitEvent(s, ev[1], 0))
+    return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 int fa_get_device_error(fa_stream_t stream) {

@@ -114,3 +114,21 @@ def test_splitkv_host_side_checks(lib):
     assert _split(lib, ws=0x40000) == FA_ERR_ALIAS           # workspace over o
     assert _split(lib, ws=0x20000) == FA_ERR_ALIAS           # workspace over k
     assert lib.fa_error_string(-11) == b"workspace smaller than fa_fwd_splitkv_workspace_size()"
+
+
+def test_fwd_host_host_side_checks(lib):
+    # Fake, never dereferenced addresses: every case below fails a host-side check first.
+    h = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000]
+    dvc = [0x10000, 0x20000, 0x30000, 0x40000, 0x50000]
+
+    def call(hosts=h, devs=dvc, B=2, H=1, N=128, d=64, dtype=0):
+        return lib.fa_fwd_host(*hosts, *devs, B, H, N, d, 0, 0.125, dtype, None)
+
+    assert call(hosts=[0] + h[1:]) == FA_ERR_NULL
+    assert call(hosts=h[:4] + [0]) == FA_ERR_NULL
+    assert call(devs=[0] + dvc[1:]) == FA_ERR_NULL
+    assert call(B=0) == FA_ERR_SHAPE
+    assert call(d=96) == FA_ERR_SHAPE
+    assert call(dtype=5) == FA_ERR_DTYPE
+    assert call(devs=[0x10008] + dvc[1:]) == FA_ERR_ALIGN
+    assert call(devs=dvc[:3] + [0x10000 + 0x100, dvc[4]]) == FA_ERR_ALIAS   # o_d over q_d

@@ -141,3 +141,27 @@ def test_user_api_host_and_device_tensors():
     assert not o_h.is_cuda and torch.equal(o_h, o_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
     o_ref, lse_ref = oracle.attention(qb, kb, vb, True, softmax_scale(64), dtype="fp16")
     assert_close(o_h.double().numpy(), lse_h.double().numpy(), o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,pinned", [
+    (1, 4, 200, 64, True, True), (3, 4, 1000, 128, False, True), (5, 4, 333, 128, True, False),
+    (2, 16, 8192, 128, True, True),     # 3 head groups of 5, 5, 6 heads
+    (3, 11, 8192, 64, False, True),     # 3 uneven groups
+    (1, 12, 16384, 128, True, False)])  # 2 groups, pageable host memory
+def test_host_entry_matches_device_path(B, H, N, d, causal, pinned):
+    """fa_fwd_host (host buffers, head groups packed by pitched copies, copies overlapping the
+    kernels) gives exactly the device path's O and LSE: the same kernel on the same values."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    qb, kb, vb = make_qkv(B, H, N, d, "bf16", seed=8100 + B + N)
+    hq, hk, hv = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) for x in (qb, kb, vb))
+    if pinned:
+        hq, hk, hv = (t.pin_memory() for t in (hq, hk, hv))
+    o_h, l_h = binding.attention_forward(hq, hk, hv, causal=causal)
+    q, k, v = (t.cuda() for t in (hq, hk, hv))
+    o_d, l_d = binding.attention_forward(q, k, v, causal=causal)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    assert torch.equal(o_h.view(torch.int16), o_d.cpu().view(torch.int16))
+    assert torch.equal(l_h, l_d.cpu())
