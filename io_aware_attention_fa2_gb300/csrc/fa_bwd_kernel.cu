@@ -635,10 +635,6 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-size_t bwd_smem_bytes(int d) {
-  return d == 64 ? BwdSmem<64>::kDynamic : BwdSmem<128>::kDynamic;
-}
-
 cudaError_t launch_bwd(const BwdParams& p, cudaStream_t stream) {
   if (p.d == 64)
     return p.fp16 ? launch_bwd_impl<64, true>(p, stream) : launch_bwd_impl<64, false>(p, stream);

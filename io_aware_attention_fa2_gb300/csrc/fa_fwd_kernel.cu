@@ -649,15 +649,6 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-size_t fwd_smem_bytes(int d) {
-  return d == 64 ? SmemLayout<64>::kDynamic : SmemLayout<128>::kDynamic;
-}
-
-long long fwd_num_ctas(int B, int H, int Nq, int num_splits) {
-  return static_cast<long long>(B) * H * ((Nq + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M)) *
-         num_splits;
-}
-
 template <bool WINDOWED>
 cudaError_t launch_dtype(const FwdParams& p, cudaStream_t stream) {
   if (p.d == 64)

@@ -40,12 +40,6 @@ struct FwdParams {
 // Enqueue the forward kernel. Returns a CUDA error (cudaSuccess when enqueued).
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
 
-// Dynamic shared memory the forward kernel needs for head dimension d.
-size_t fwd_smem_bytes(int d);
-
-// Number of CTAs (one per 256-row Q block of every (b, h) and K/V part) the forward launches.
-long long fwd_num_ctas(int B, int H, int Nq, int num_splits);
-
 // Device error word of the current device: read (after synchronising `stream`) and clear.
 cudaError_t read_and_clear_device_error(cudaStream_t stream, int* value);
 
@@ -67,7 +61,6 @@ struct BwdParams {
 
 // Enqueue the backward (pre-kernel, main kernel, post-kernel).
 cudaError_t launch_bwd(const BwdParams& p, cudaStream_t stream);
-size_t bwd_smem_bytes(int d);
 // The backward kernels' error word of the current device: read and clear (no synchronisation).
 cudaError_t read_and_clear_bwd_error(int* value);
 
