@@ -83,12 +83,14 @@ def test_bwd_bad_arguments():
 
 
 @pytest.mark.parametrize("name,heads", [("n8k_d128_causal", [(0, 3), (1, 12)]),
-                                        ("n8k_d128", [(1, 7)])])
+                                        ("n8k_d128", [(1, 7)]),
+                                        ("n2000_d128_fp16_stress", [(0, 0), (15, 31)]),
+                                        ("n1k_d64_causal", [(3, 15)])])
 def test_bwd_full_size_sampled(name, heads):
-    """The benchmarked shape (B=2, H=16, N=8192, d=128 bf16) with the bench's upstream gradient,
-    one fa_bwd call as the bench launches it; dQ, dK, dV compared on sampled positions (tile
-    edges, the middle, the last row and seeded ones) of the given heads against the sampled
-    fp64 oracle."""
+    """Full-size workloads (the benchmarked B=2, H=16, N=8192, d=128 bf16 shape, the fp16 stress
+    shape with its large logits, d=64) with the bench's upstream gradient, one fa_bwd call as
+    the bench launches it; dQ, dK, dV compared on sampled positions (tile edges, the middle,
+    the last row and seeded ones) of the given heads against the sampled fp64 oracle."""
     import torch
 
     from io_aware_attention_fa2_gb300 import binding
