@@ -227,6 +227,17 @@ const char* fa_error_string(int code);
  */
 int fa_get_device_error(fa_stream_t stream);
 
+/*
+ * fa_selftest_wait_timeout -- diagnostic for the failure path every kernel wait shares: enqueues
+ * on `stream` one warp that waits, with the kernels' own bounded wait, on a barrier nothing ever
+ * completes, for `limit_us` microseconds (1 .. 1e6); the wait runs out, the kernel records
+ * FA_ERR_TIMEOUT in the device error word and exits. fa_get_device_error(stream) then returns
+ * FA_ERR_TIMEOUT (and clears it), and the device stays usable. (Not on the pages: a check of
+ * this library's error reporting.) Returns FA_OK once enqueued, FA_ERR_SHAPE for a limit out of
+ * range, FA_ERR_ARCH / FA_ERR_CUDA / FA_ERR_LAUNCH as fa_fwd.
+ */
+int fa_selftest_wait_timeout(int limit_us, fa_stream_t stream);
+
 /* ABI version of this header: 1. */
 int fa_abi_version(void);
 

@@ -70,6 +70,8 @@ def load_library() -> ctypes.CDLL:
             lib.fa_error_string.restype = ctypes.c_char_p
             lib.fa_get_device_error.argtypes = [vp]
             lib.fa_get_device_error.restype = i32
+            lib.fa_selftest_wait_timeout.argtypes = [i32, vp]
+            lib.fa_selftest_wait_timeout.restype = i32
             lib.fa_abi_version.argtypes = []
             lib.fa_abi_version.restype = i32
             _lib = lib

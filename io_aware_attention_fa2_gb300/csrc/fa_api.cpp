@@ -350,6 +350,17 @@ int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, fl
   return FA_OK;
 }
 
+int fa_selftest_wait_timeout(int limit_us, fa_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return FA_ERR_SHAPE;
+  int device = 0;
+  const int rc = check_arch(&device);
+  if (rc != FA_OK) return rc;
+  if (fa::launch_selftest_wait(1000ull * (unsigned long long)limit_us,
+                               reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  return FA_OK;
+}
+
 int fa_get_device_error(fa_stream_t stream) {
   int value = 0, bwd_value = 0;
   if (fa::read_and_clear_device_error(reinterpret_cast<cudaStream_t>(stream), &value) !=

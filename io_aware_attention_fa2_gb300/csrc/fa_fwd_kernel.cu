@@ -663,6 +663,30 @@ cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
   return windowed ? launch_dtype<true>(p, stream) : launch_dtype<false>(p, stream);
 }
 
+namespace {
+
+// Diagnostic: one thread waits, with the kernels' own bounded wait, on an mbarrier that nothing
+// ever arrives on, and records the timeout in the error word exactly as the attention kernels
+// do. It exercises the failure path (wait runs out -> error word -> host) without a fault.
+__global__ void __launch_bounds__(32) fa_selftest_wait_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t never;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    ptx::mbar_init(ptx::smem_addr(&never), 1);
+    ptx::fence_barrier_init();
+    if (!ptx::wait_bounded(ptx::smem_addr(&never), 0, &abort_flag, limit_ns))
+      record_timeout(&abort_flag);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream) {
+  fa_selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_device_error(cudaStream_t stream, int* value) {
   cudaError_t err = cudaStreamSynchronize(stream);
   if (err != cudaSuccess) return err;

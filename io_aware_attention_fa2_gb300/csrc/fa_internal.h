@@ -43,6 +43,9 @@ cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
 // Device error word of the current device: read (after synchronising `stream`) and clear.
 cudaError_t read_and_clear_device_error(cudaStream_t stream, int* value);
 
+// The bounded-wait self-test kernel (a wait on an mbarrier nothing arrives on).
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
+
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;   // [B, N, H, d] as in FwdParams
   const void* o;        // [B, N, H, d] forward output

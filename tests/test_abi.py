@@ -132,3 +132,11 @@ def test_fwd_host_host_side_checks(lib):
     assert call(dtype=5) == FA_ERR_DTYPE
     assert call(devs=[0x10008] + dvc[1:]) == FA_ERR_ALIGN
     assert call(devs=dvc[:3] + [0x10000 + 0x100, dvc[4]]) == FA_ERR_ALIAS   # o_d over q_d
+
+
+def test_selftest_wait_timeout_host_checks(lib):
+    assert lib.fa_selftest_wait_timeout(0, None) == FA_ERR_SHAPE
+    assert lib.fa_selftest_wait_timeout(2000001, None) == FA_ERR_SHAPE
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.fa_selftest_wait_timeout(1000, None) in (FA_ERR_CUDA, FA_ERR_ARCH)
