@@ -9,10 +9,11 @@ Importing the package does not load the CUDA library; the first call does, and r
 library has not been built (there is no fallback path).
 """
 from .binding import (FaError, attention_backward, attention_forward, available,
-                      bwd_workspace_size,
-                      device_error, error_string, fa_bwd, fa_fwd, fa_fwd_splitkv, library_path,
-                      load_library, splitkv_num_splits, splitkv_workspace_size)
+                      bwd_workspace_size, device_error, error_string, fa_bwd, fa_fwd,
+                      fa_fwd_splitkv, library_path, load_library, splitkv_num_splits,
+                      splitkv_workspace_size)
 
-__all__ = ["FaError", "attention_backward", "attention_forward", "available", "bwd_workspace_size", "device_error",
-           "error_string", "fa_bwd", "fa_fwd", "fa_fwd_splitkv", "library_path", "load_library", "splitkv_num_splits",
+__all__ = ["FaError", "attention_backward", "attention_forward", "available",
+           "bwd_workspace_size", "device_error", "error_string", "fa_bwd", "fa_fwd",
+           "fa_fwd_splitkv", "library_path", "load_library", "splitkv_num_splits",
            "splitkv_workspace_size"]

@@ -166,7 +166,8 @@ def splitkv_num_splits(B: int, H: int, Nq: int, Nk: int, num_sms: int | None = N
     the current device's)."""
     if num_sms is None:
         import torch
-        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        props = torch.cuda.get_device_properties(torch.cuda.current_device())
+        num_sms = props.multi_processor_count
     return int(load_library().fa_fwd_splitkv_num_splits(B, H, Nq, Nk, num_sms))
 
 

@@ -20,8 +20,9 @@
 //   dP^T = V_j dO_i^T    (smem x smem)            -> T_dP
 //   softmax warps: P^T = exp2(S^T scale log2e - LSE_i log2e) (masked), written back over T_S
 //                  as 16-bit pairs and read back from there for dS^T = P^T (dP^T - D_i),
-//                  stored as rows (queries contiguous, 128-byte swizzle) in shared memory. The factor scale of dS' = scale dS is
-//                  applied to dK in its epilogue and to dQ when it is rounded.
+//                  stored as rows (queries contiguous, 128-byte swizzle) in shared memory.
+//                  The factor scale of dS' = scale dS is applied to dK in its epilogue and
+//                  to dQ when it is rounded.
 //   dV  += P^T dO_i      (TMEM x smem, dO MN-major)
 //   dQ_i^T = K_j^T dS^T  (smem x smem, both MN-major; d = 128)  -> T_dP, lanes = features
 //   (d = 64: dQ_i = dS K_j, lanes = queries)
