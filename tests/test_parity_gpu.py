@@ -165,3 +165,40 @@ def test_host_entry_matches_device_path(B, H, N, d, causal, pinned):
     assert binding.device_error() == 0
     assert torch.equal(o_h.view(torch.int16), o_d.cpu().view(torch.int16))
     assert torch.equal(l_h, l_d.cpu())
+
+
+def test_many_small_heads_full():
+    """B x H = 2048 heads of 128 rows (2048 units of one Q tile each, many dispatch groups),
+    every output row against the oracle."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    B, H, N, d = 64, 32, 128, 64
+    qb, kb, vb = make_qkv(B, H, N, d, "bf16", seed=8300)
+    q, k, v = (to_device(x, "bf16") for x in (qb, kb, vb))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    binding.fa_fwd(q, k, v, o, lse, True, softmax_scale(d))
+    assert binding.device_error() == 0
+    o_ref, lse_ref = oracle.attention(qb, kb, vb, True, softmax_scale(d), dtype="bf16")
+    assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), o_ref, lse_ref,
+                 "64x32 heads of 128")
+
+
+def test_long_sequence_d64_sampled():
+    """N = 32768 with d = 64 (256 K/V tiles for the last Q block), causal; sampled rows."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    B, H, N, d = 1, 2, 32768, 64
+    qb, kb, vb = make_qkv(B, H, N, d, "bf16", seed=8400)
+    q, k, v = (to_device(x, "bf16") for x in (qb, kb, vb))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    binding.fa_fwd(q, k, v, o, lse, True, softmax_scale(d))
+    assert binding.device_error() == 0
+    rows = sample_rows(B, H, N, 48, seed=8401)
+    o_ref, lse_ref = oracle.attention_rows(qb, kb, vb, rows, True, softmax_scale(d), dtype="bf16")
+    rb, rh, ri = (torch.from_numpy(rows[:, c]).cuda() for c in range(3))
+    assert_close(o[rb, ri, rh].double().cpu().numpy(), lse[rb, rh, ri].double().cpu().numpy(),
+                 o_ref, lse_ref, "N=32768 d=64")
