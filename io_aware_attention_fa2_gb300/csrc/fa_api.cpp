@@ -287,15 +287,27 @@ int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, fl
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
   // Chunks: groups of heads across all batches, packed by pitched copies into a compact
-  // [B, N, heads, d] problem in the device buffers and unpacked the same way. As many groups as
-  // keep two waves of work units (b, h, 256-row Q block) per chunk, at most kHostChunks * 2.
+  // [B, N, heads, d] problem in the device buffers and unpacked the same way. When the copies
+  // clearly dominate (kernel time estimated below half the copy time, at ~1 PFLOP/s against
+  // ~200 GB/s over the host link), as many groups as allowed: the last group's kernel and
+  // output copy are all that is not overlapped. Otherwise as many
+  // as keep two waves of work units (b, h, 256-row Q block) per group, so that no group's
+  // kernel leaves SMs idle.
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
       sms < 1)
     return FA_ERR_CUDA;
   const long long units = (long long)B * H * ((N + 255) / 256);
+  const double flops = 4.0 * B * H * (double)N * N * d * (causal ? 0.5 : 1.0);
+  const double copy_bytes = 4.0 * B * H * (double)N * d * 2 + (double)B * H * N * 4;
+  const bool copy_bound = flops / 1e15 < 0.5 * copy_bytes / 200e9;
+  // at most H groups and kHostChunks * 2, each with at least 16 MB of copies (below that, the
+  // per-group launch and copy set-up costs more than the overlap saves)
+  const long long max_chunks = std::max<long long>(
+      1, std::min<long long>({(long long)H, 2ll * kHostChunks,
+                              (long long)(copy_bytes / (16.0 * (1 << 20)))}));
   const int chunks = (int)std::max<long long>(
-      1, std::min<long long>({(long long)H, 2ll * kHostChunks, units / (2ll * sms)}));
+      1, copy_bound ? max_chunks : std::min<long long>(max_chunks, units / (2ll * sms)));
   std::lock_guard<std::mutex> lock(g_host_mutex);
   HostPipe* hp = nullptr;
   rc = host_pipe(device, 2 + 2 * (size_t)chunks, &hp);
