@@ -217,6 +217,30 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 /* Bytes of workspace fa_bwd needs: B*H*N*(d + 1)*4. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
+/*
+ * fa_bwd_host -- fa_bwd on host buffers, in the manner of fa_fwd_host: q, k, v, o, dout and
+ * lse are copied to device buffers group of heads by group of heads, fa_bwd runs on each group
+ * packed into a compact problem, and dQ, dK, dV are copied back, so that the copies of one
+ * group overlap the computation of another. (No counterpart in the pages; the end-to-end form
+ * of fa_bwd for data that lives in host memory.)
+ *
+ *   q_h, k_h, v_h, o_h, do_h  [B, N, H, d] dtype, host memory: inputs (do_h is dO)
+ *   lse_h          [B, H, N] fp32, host memory: the forward's LSE
+ *   dq_h, dk_h, dv_h  [B, N, H, d] dtype, host memory: outputs
+ *   q_d ... dv_d   device buffers of the same sizes, owned by the caller, pairwise disjoint,
+ *                  16-byte aligned (lse_d 4-byte); their previous contents are overwritten
+ *   workspace      as in fa_bwd for the whole problem (every group reuses it in turn)
+ *   B, H, N, d, causal, scale, dtype: as in fa_bwd
+ * Streams, pinned memory, synchronisation and errors as in fa_fwd_host: synchronise `stream`
+ * before reading dq_h, dk_h, dv_h.
+ */
+int fa_bwd_host(const void* q_h, const void* k_h, const void* v_h, const void* o_h,
+                const void* do_h, const float* lse_h, void* dq_h, void* dk_h, void* dv_h,
+                void* q_d, void* k_d, void* v_d, void* o_d, void* do_d, float* lse_d,
+                void* dq_d, void* dk_d, void* dv_d, void* workspace, size_t workspace_bytes,
+                int B, int H, int N, int d, int causal, float scale, int dtype,
+                fa_stream_t stream);
+
 /* Static English text for a status code (never NULL). */
 const char* fa_error_string(int code);
 

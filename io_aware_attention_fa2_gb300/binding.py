@@ -64,6 +64,9 @@ def load_library() -> ctypes.CDLL:
             lib.fa_bwd.restype = i32
             lib.fa_fwd_host.argtypes = [vp] * 10 + [i32, i32, i32, i32, i32, f32, i32, vp]
             lib.fa_fwd_host.restype = i32
+            lib.fa_bwd_host.argtypes = [vp] * 19 + [ctypes.c_size_t] + [i32] * 5 + [f32, i32,
+                                                                              vp]
+            lib.fa_bwd_host.restype = i32
             lib.fa_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
             lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
             lib.fa_error_string.argtypes = [i32]
@@ -294,7 +297,8 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
              and q.dtype in (torch.bfloat16, torch.float16) and k.dtype == q.dtype
              and v.dtype == q.dtype and o_host.dtype == q.dtype)
     if plain:
-        # fa_fwd_host: the library copies batch by batch, overlapping copies and compute.
+        # fa_fwd_host: the library copies group of heads by group of heads, overlapping
+        # the copies of one group with the kernel of another.
         with torch.cuda.device(dev):
             qd, kd, vd, od = (torch.empty(q.shape, dtype=q.dtype, device=dev) for _ in range(4))
             ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -335,14 +339,28 @@ def attention_backward(q, k, v, o, dout, lse, causal: bool = False, scale: float
         dq, dk, dv = (torch.empty_like(q) for _ in range(3))
         fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal, scale, None, stream)
         return dq, dk, dv
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != q.dtype or t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous host tensor like q" % name)
+    if (q.dtype not in (torch.bfloat16, torch.float16) or not q.is_contiguous()
+            or lse.shape != (B, H, N) or lse.dtype != torch.float32 or lse.is_cuda
+            or not lse.is_contiguous()):
+        raise ValueError("q must be a contiguous bf16/fp16 host tensor, lse float32 [B, H, N]")
     dev = torch.device(device or "cuda:0")
     st = stream if stream is not None else torch.cuda.current_stream(dev)
-    with torch.cuda.stream(st):
-        dev_in = [t.to(dev, non_blocking=True) for t in (q, k, v, o, dout, lse)]
-        grads = [torch.empty_like(dev_in[0]) for _ in range(3)]
-        fa_bwd(*dev_in, *grads, causal, scale, None, st)
-        host = [torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned()) for _ in range(3)]
-        for h_, g_ in zip(host, grads):
-            h_.copy_(g_, non_blocking=True)
+    host = [torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned()) for _ in range(3)]
+    with torch.cuda.device(dev):
+        bufs = [torch.empty(q.shape, dtype=q.dtype, device=dev) for _ in range(8)]
+        ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        need = bwd_workspace_size(B, H, N, d)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    # fa_bwd_host: copies of one group of heads overlap the kernels of another
+    rc = load_library().fa_bwd_host(
+        *(t.data_ptr() for t in (q, k, v, o, dout, lse, *host)),
+        *(t.data_ptr() for t in bufs[:5]), ld.data_ptr(), *(t.data_ptr() for t in bufs[5:]),
+        ws.data_ptr(), need, B, H, N, d, int(bool(causal)), float(scale), _dtype_code(q),
+        st.cuda_stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_host")
     st.synchronize()
     return tuple(host)

@@ -110,7 +110,8 @@ namespace {
 // Host-side checks shared by every forward entry point (nothing is enqueued).
 int check_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                   int H, int Nq, int Nk, int d, int dtype, float scale, const int* seqlens_k,
-                  int num_splits, void* workspace, size_t workspace_bytes) {
+                  int num_splits, void* workspace, size_t workspace_bytes,
+                  bool inputs_written = false) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (B < 1 || H < 1 || Nq < 1 || Nk < Nq || (d != 64 && d != 128)) return FA_ERR_SHAPE;
   if (num_splits < 1 || num_splits > fa::MAX_SPLITS) return FA_ERR_SHAPE;
@@ -150,6 +151,11 @@ int check_forward(const void* q, const void* k, const void* v, void* o, float* l
     for (int j = i + 1; j < 3; ++j)
       if (outs[i].p && outs[j].p && overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n))
         return FA_ERR_ALIAS;
+  // the host-buffer entry points copy into the input buffers, so these may not share memory
+  if (inputs_written)
+    for (int i = 0; i < 3; ++i)
+      for (int j = i + 1; j < 3; ++j)
+        if (overlaps(ins[i].p, ins[i].n, ins[j].p, ins[j].n)) return FA_ERR_ALIAS;
   int device = 0;
   return check_arch(&device);
 }
@@ -246,6 +252,50 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 
 namespace {
 
+// Host-side checks of fa_bwd (nothing is enqueued).
+int check_backward(const void* q, const void* k, const void* v, const void* o,
+                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                   int H, int N, int d, float scale, int dtype, void* workspace,
+                   size_t workspace_bytes, bool inputs_written = false) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+    return FA_ERR_NULL;
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return FA_ERR_SHAPE;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
+  if (!isfinite(scale)) return FA_ERR_SCALE;
+  const uint64_t bh = (uint64_t)B * (uint64_t)H;
+  if (bh * (uint64_t)((N + 127) / 128) >= (1ull << 31)) return FA_ERR_SHAPE;
+  const uint64_t elems = bh * (uint64_t)N * (uint64_t)d;
+  if (elems > (1ull << 62) / 4) return FA_ERR_SHAPE;
+  if (workspace_bytes < fa_bwd_workspace_size(B, H, N, d)) return FA_ERR_WORKSPACE;
+  const uint64_t t_bytes = elems * 2, lse_bytes = bh * (uint64_t)N * 4;
+  for (const void* p : {q, k, v, o, dout, static_cast<const void*>(dq),
+                        static_cast<const void*>(dk), static_cast<const void*>(dv),
+                        static_cast<const void*>(workspace)})
+    if (reinterpret_cast<uintptr_t>(p) % 16) return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) % 4) return FA_ERR_ALIGN;
+  struct Span { const void* p; uint64_t n; };
+  const Span ins[] = {{q, t_bytes}, {k, t_bytes}, {v, t_bytes}, {o, t_bytes}, {dout, t_bytes},
+                      {lse, lse_bytes}};
+  const Span outs[] = {{dq, t_bytes}, {dk, t_bytes}, {dv, t_bytes},
+                       {workspace, fa_bwd_workspace_size(B, H, N, d)}};
+  for (const Span& out : outs)
+    for (const Span& in : ins)
+      if (overlaps(out.p, out.n, in.p, in.n)) return FA_ERR_ALIAS;
+  for (int i = 0; i < 4; ++i)
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return FA_ERR_ALIAS;
+  if (inputs_written)   // as in check_forward
+    for (int i = 0; i < 6; ++i)
+      for (int j = i + 1; j < 6; ++j)
+        if (overlaps(ins[i].p, ins[i].n, ins[j].p, ins[j].n)) return FA_ERR_ALIAS;
+  int device = 0;
+  return check_arch(&device);
+}
+
+}  // namespace
+
+namespace {
+
 // Per device: the two copy streams of fa_fwd_host and its events, created on first use and
 // kept for the life of the process. One mutex serialises the enqueueing of fa_fwd_host calls,
 // so that two callers never interleave their event records and waits.
@@ -273,6 +323,52 @@ int host_pipe(int device, size_t events, HostPipe** out) {
 
 constexpr int kHostChunks = 4;   // up to 2 * kHostChunks chunks per call
 
+// Number of head groups a host-buffer call is cut into (the groups' copies overlap the kernels
+// of other groups). At most H and 2 * kHostChunks, each with at least 16 MB of copies (below
+// that, the per-group launch and copy set-up costs more than the overlap saves). When the
+// copies clearly dominate (kernel time estimated below half the copy time, at ~1 PFLOP/s
+// against ~200 GB/s over the host link), as many groups as allowed: the last group's kernel
+// and output copies are all that is not overlapped. Otherwise as many as keep two waves of
+// `units` (the kernel's CTAs for the whole problem) per group, so that no group's kernel leaves
+// SMs idle.
+int host_groups(int device, int H, long long units, double flops, double copy_bytes,
+                int* groups) {
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      sms < 1)
+    return FA_ERR_CUDA;
+  const bool copy_bound = flops / 1e15 < 0.5 * copy_bytes / 200e9;
+  const long long max_groups = std::max<long long>(
+      1, std::min<long long>({(long long)H, 2ll * kHostChunks,
+                              (long long)(copy_bytes / (16.0 * (1 << 20)))}));
+  *groups = (int)std::max<long long>(
+      1, copy_bound ? max_groups : std::min<long long>(max_groups, units / (2ll * sms)));
+  return FA_OK;
+}
+
+// Heads [h0, h0 + hc) of a [B, N, H, d] 16-bit array between host memory (pitch H * d) and a
+// compact [B, N, hc, d] device array, as one pitched copy.
+bool copy_heads(void* compact, void* host, bool to_device, int B, int N, int H, int h0, int hc,
+                int d, cudaStream_t st) {
+  const size_t row = (size_t)d * 2, width = (size_t)hc * row, pitch = (size_t)H * row;
+  char* h = static_cast<char*>(host) + (size_t)h0 * row;
+  return (to_device ? cudaMemcpy2DAsync(compact, width, h, pitch, width, (size_t)B * N,
+                                        cudaMemcpyHostToDevice, st)
+                    : cudaMemcpy2DAsync(h, pitch, compact, width, width, (size_t)B * N,
+                                        cudaMemcpyDeviceToHost, st)) == cudaSuccess;
+}
+
+// The same for a [B, H, N] fp32 array (LSE): B blocks of hc * N floats.
+bool copy_rows(float* compact, float* host, bool to_device, int B, int N, int H, int h0, int hc,
+               cudaStream_t st) {
+  const size_t width = (size_t)hc * N * 4, pitch = (size_t)H * N * 4;
+  float* h = host + (size_t)h0 * N;
+  return (to_device ? cudaMemcpy2DAsync(compact, width, h, pitch, width, (size_t)B,
+                                        cudaMemcpyHostToDevice, st)
+                    : cudaMemcpy2DAsync(h, pitch, compact, width, width, (size_t)B,
+                                        cudaMemcpyDeviceToHost, st)) == cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -282,81 +378,115 @@ int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, fl
                 int d, int causal, float scale, int dtype, fa_stream_t stream) {
   if (!q_h || !k_h || !v_h || !o_h || !lse_h) return FA_ERR_NULL;
   int rc = check_forward(q_d, k_d, v_d, o_d, lse_d, B, H, N, N, d, dtype, scale, nullptr, 1,
-                         nullptr, 0);
+                         nullptr, 0, true);
   if (rc != FA_OK) return rc;
-  int device = 0;
+  int device = 0, groups = 1;
   if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
-  // Chunks: groups of heads across all batches, packed by pitched copies into a compact
-  // [B, N, heads, d] problem in the device buffers and unpacked the same way. When the copies
-  // clearly dominate (kernel time estimated below half the copy time, at ~1 PFLOP/s against
-  // ~200 GB/s over the host link), as many groups as allowed: the last group's kernel and
-  // output copy are all that is not overlapped. Otherwise as many
-  // as keep two waves of work units (b, h, 256-row Q block) per group, so that no group's
-  // kernel leaves SMs idle.
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-      sms < 1)
-    return FA_ERR_CUDA;
-  const long long units = (long long)B * H * ((N + 255) / 256);
-  const double flops = 4.0 * B * H * (double)N * N * d * (causal ? 0.5 : 1.0);
-  const double copy_bytes = 4.0 * B * H * (double)N * d * 2 + (double)B * H * N * 4;
-  const bool copy_bound = flops / 1e15 < 0.5 * copy_bytes / 200e9;
-  // at most H groups and kHostChunks * 2, each with at least 16 MB of copies (below that, the
-  // per-group launch and copy set-up costs more than the overlap saves)
-  const long long max_chunks = std::max<long long>(
-      1, std::min<long long>({(long long)H, 2ll * kHostChunks,
-                              (long long)(copy_bytes / (16.0 * (1 << 20)))}));
-  const int chunks = (int)std::max<long long>(
-      1, copy_bound ? max_chunks : std::min<long long>(max_chunks, units / (2ll * sms)));
+  rc = host_groups(device, H, (long long)B * H * ((N + 255) / 256),
+                   4.0 * B * H * (double)N * N * d * (causal ? 0.5 : 1.0),
+                   4.0 * B * H * (double)N * d * 2 + (double)B * H * N * 4, &groups);
+  if (rc != FA_OK) return rc;
   std::lock_guard<std::mutex> lock(g_host_mutex);
   HostPipe* hp = nullptr;
-  rc = host_pipe(device, 2 + 2 * (size_t)chunks, &hp);
+  rc = host_pipe(device, 2 + 2 * (size_t)groups, &hp);
   if (rc != FA_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaEvent_t* ev = hp->events.data();   // [0] start, [1] end, then in/kernel per chunk
+  cudaEvent_t* ev = hp->events.data();   // [0] start, [1] end, then in/kernel per group
   // The copy streams start after the work already on `stream`.
   if (cudaEventRecord(ev[0], s) != cudaSuccess || cudaStreamWaitEvent(hp->in, ev[0], 0) ||
       cudaStreamWaitEvent(hp->out, ev[0], 0))
     return FA_ERR_CUDA;
-  const uint64_t head_row = (uint64_t)d * 2;                // bytes of one (b, n, h) row
-  const uint64_t hpitch = (uint64_t)H * head_row, height = (uint64_t)B * N;
-  uint64_t packed = 0, packed_lse = 0;                      // bytes / floats placed so far
-  for (int c = 0; c < chunks; ++c) {
-    const int h0 = (int)((int64_t)H * c / chunks), h1 = (int)((int64_t)H * (c + 1) / chunks);
+  // Group g: heads [h0, h1) of every batch, packed into a compact [B, N, h1 - h0, d] problem
+  // at the next free offset of the device buffers.
+  size_t packed = 0, packed_lse = 0;   // bytes / floats used so far
+  for (int g = 0; g < groups; ++g) {
+    const int h0 = (int)((int64_t)H * g / groups), h1 = (int)((int64_t)H * (g + 1) / groups);
     const int hc = h1 - h0;
-    const uint64_t width = (uint64_t)hc * head_row;
     char* qd = static_cast<char*>(q_d) + packed;
     char* kd = static_cast<char*>(k_d) + packed;
     char* vd = static_cast<char*>(v_d) + packed;
     char* od = static_cast<char*>(o_d) + packed;
     float* ld = lse_d + packed_lse;
-    const uint64_t host_off = (uint64_t)h0 * head_row;      // row (b, n) = (0, 0), head h0
-    cudaEvent_t ev_in = ev[2 + 2 * c], ev_k = ev[3 + 2 * c];
-    for (int t = 0; t < 3; ++t) {
-      const char* src = static_cast<const char*>(t == 0 ? q_h : t == 1 ? k_h : v_h) + host_off;
-      char* dst = t == 0 ? qd : t == 1 ? kd : vd;
-      if (cudaMemcpy2DAsync(dst, width, src, hpitch, width, height, cudaMemcpyHostToDevice,
-                            hp->in) != cudaSuccess)
-        return FA_ERR_CUDA;
-    }
-    if (cudaEventRecord(ev_in, hp->in) != cudaSuccess || cudaStreamWaitEvent(s, ev_in, 0))
+    if (!copy_heads(qd, const_cast<void*>(q_h), true, B, N, H, h0, hc, d, hp->in) ||
+        !copy_heads(kd, const_cast<void*>(k_h), true, B, N, H, h0, hc, d, hp->in) ||
+        !copy_heads(vd, const_cast<void*>(v_h), true, B, N, H, h0, hc, d, hp->in) ||
+        cudaEventRecord(ev[2 + 2 * g], hp->in) != cudaSuccess ||
+        cudaStreamWaitEvent(s, ev[2 + 2 * g], 0) != cudaSuccess)
       return FA_ERR_CUDA;
     rc = run_forward(qd, kd, vd, od, ld, B, hc, N, N, d, causal, -1, -1, nullptr, scale, dtype,
                      1, nullptr, 0, stream);
     if (rc != FA_OK) return rc;
-    if (cudaEventRecord(ev_k, s) != cudaSuccess || cudaStreamWaitEvent(hp->out, ev_k, 0) ||
-        cudaMemcpy2DAsync(static_cast<char*>(o_h) + host_off, hpitch, od, width, width, height,
-                          cudaMemcpyDeviceToHost, hp->out) != cudaSuccess)
+    if (cudaEventRecord(ev[3 + 2 * g], s) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->out, ev[3 + 2 * g], 0) != cudaSuccess ||
+        !copy_heads(od, o_h, false, B, N, H, h0, hc, d, hp->out) ||
+        !copy_rows(ld, lse_h, false, B, N, H, h0, hc, hp->out))
       return FA_ERR_CUDA;
-    // LSE rows (b, h) of the chunk: hc * N floats per batch, at (b * H + h0) * N in lse_h
-    if (cudaMemcpy2DAsync(lse_h + (uint64_t)h0 * N, (uint64_t)H * N * 4, ld,
-                          (uint64_t)hc * N * 4, (uint64_t)hc * N * 4, (uint64_t)B,
-                          cudaMemcpyDeviceToHost, hp->out) != cudaSuccess)
-      return FA_ERR_CUDA;
-    packed += width * height;
-    packed_lse += (uint64_t)B * hc * N;
+    packed += (size_t)B * N * hc * d * 2;
+    packed_lse += (size_t)B * hc * N;
   }
   // `stream` reaches this point once the last output copy is done.
+  if (cudaEventRecord(ev[1], hp->out) != cudaSuccess || cudaStreamWaitEvent(s, ev[1], 0))
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+int fa_bwd_host(const void* q_h, const void* k_h, const void* v_h, const void* o_h,
+                const void* do_h, const float* lse_h, void* dq_h, void* dk_h, void* dv_h,
+                void* q_d, void* k_d, void* v_d, void* o_d, void* do_d, float* lse_d,
+                void* dq_d, void* dk_d, void* dv_d, void* workspace, size_t workspace_bytes,
+                int B, int H, int N, int d, int causal, float scale, int dtype,
+                fa_stream_t stream) {
+  if (!q_h || !k_h || !v_h || !o_h || !do_h || !lse_h || !dq_h || !dk_h || !dv_h)
+    return FA_ERR_NULL;
+  int rc = check_backward(q_d, k_d, v_d, o_d, do_d, lse_d, dq_d, dk_d, dv_d, B, H, N, d, scale,
+                          dtype, workspace, workspace_bytes, true);
+  if (rc != FA_OK) return rc;
+  int device = 0, groups = 1;
+  if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
+  rc = host_groups(device, H, (long long)B * H * ((N + 127) / 128),
+                   2.5 * 4.0 * B * H * (double)N * N * d * (causal ? 0.5 : 1.0),
+                   8.0 * B * H * (double)N * d * 2 + (double)B * H * N * 4, &groups);
+  if (rc != FA_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_host_mutex);
+  HostPipe* hp = nullptr;
+  rc = host_pipe(device, 2 + 2 * (size_t)groups, &hp);
+  if (rc != FA_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaEvent_t* ev = hp->events.data();
+  if (cudaEventRecord(ev[0], s) != cudaSuccess || cudaStreamWaitEvent(hp->in, ev[0], 0) ||
+      cudaStreamWaitEvent(hp->out, ev[0], 0))
+    return FA_ERR_CUDA;
+  // Each group's fa_bwd runs on `stream` after the previous group's, so all of them can use
+  // the start of the workspace (a group needs at most what the whole problem needs).
+  size_t packed = 0, packed_lse = 0;
+  for (int g = 0; g < groups; ++g) {
+    const int h0 = (int)((int64_t)H * g / groups), h1 = (int)((int64_t)H * (g + 1) / groups);
+    const int hc = h1 - h0;
+    char* dev[8];
+    void* bases[8] = {q_d, k_d, v_d, o_d, do_d, dq_d, dk_d, dv_d};
+    for (int t = 0; t < 8; ++t) dev[t] = static_cast<char*>(bases[t]) + packed;
+    float* ld = lse_d + packed_lse;
+    const void* ins[5] = {q_h, k_h, v_h, o_h, do_h};
+    bool ok = true;
+    for (int t = 0; t < 5 && ok; ++t)
+      ok = copy_heads(dev[t], const_cast<void*>(ins[t]), true, B, N, H, h0, hc, d, hp->in);
+    if (!ok || !copy_rows(ld, const_cast<float*>(lse_h), true, B, N, H, h0, hc, hp->in) ||
+        cudaEventRecord(ev[2 + 2 * g], hp->in) != cudaSuccess ||
+        cudaStreamWaitEvent(s, ev[2 + 2 * g], 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+    rc = fa_bwd(dev[0], dev[1], dev[2], dev[3], dev[4], ld, dev[5], dev[6], dev[7], B, hc, N, d,
+                causal, scale, dtype, workspace, workspace_bytes, stream);
+    if (rc != FA_OK) return rc;
+    void* outs[3] = {dq_h, dk_h, dv_h};
+    if (cudaEventRecord(ev[3 + 2 * g], s) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->out, ev[3 + 2 * g], 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+    for (int t = 0; t < 3; ++t)
+      if (!copy_heads(dev[5 + t], outs[t], false, B, N, H, h0, hc, d, hp->out))
+        return FA_ERR_CUDA;
+    packed += (size_t)B * N * hc * d * 2;
+    packed_lse += (size_t)B * hc * N;
+  }
   if (cudaEventRecord(ev[1], hp->out) != cudaSuccess || cudaStreamWaitEvent(s, ev[1], 0))
     return FA_ERR_CUDA;
   return FA_OK;
@@ -388,41 +518,18 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return (size_t)(rows * (uint64_t)d * 4 + rows * 4);
 }
 
+}  // extern "C"
+
+extern "C" {
+
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
            const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
            int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
            fa_stream_t stream) {
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
-    return FA_ERR_NULL;
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return FA_ERR_SHAPE;
-  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
-  if (!isfinite(scale)) return FA_ERR_SCALE;
-  const uint64_t bh = (uint64_t)B * (uint64_t)H;
-  if (bh * (uint64_t)((N + 127) / 128) >= (1ull << 31)) return FA_ERR_SHAPE;
-  const uint64_t elems = bh * (uint64_t)N * (uint64_t)d;
-  if (elems > (1ull << 62) / 4) return FA_ERR_SHAPE;
-  if (workspace_bytes < fa_bwd_workspace_size(B, H, N, d)) return FA_ERR_WORKSPACE;
-  const uint64_t t_bytes = elems * 2, lse_bytes = bh * (uint64_t)N * 4;
-  for (const void* p : {q, k, v, o, dout, static_cast<const void*>(dq),
-                        static_cast<const void*>(dk), static_cast<const void*>(dv),
-                        static_cast<const void*>(workspace)})
-    if (reinterpret_cast<uintptr_t>(p) % 16) return FA_ERR_ALIGN;
-  if (reinterpret_cast<uintptr_t>(lse) % 4) return FA_ERR_ALIGN;
-  struct Span { const void* p; uint64_t n; };
-  const Span ins[] = {{q, t_bytes}, {k, t_bytes}, {v, t_bytes}, {o, t_bytes}, {dout, t_bytes},
-                      {lse, lse_bytes}};
-  const Span outs[] = {{dq, t_bytes}, {dk, t_bytes}, {dv, t_bytes},
-                       {workspace, fa_bwd_workspace_size(B, H, N, d)}};
-  for (const Span& out : outs)
-    for (const Span& in : ins)
-      if (overlaps(out.p, out.n, in.p, in.n)) return FA_ERR_ALIAS;
-  for (int i = 0; i < 4; ++i)
-    for (int j = i + 1; j < 4; ++j)
-      if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return FA_ERR_ALIAS;
-
-  int device = 0;
-  int rc = check_arch(&device);
+  const int rc = check_backward(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, dtype,
+                                workspace, workspace_bytes);
   if (rc != FA_OK) return rc;
+  const uint64_t elems = (uint64_t)B * (uint64_t)H * (uint64_t)N * (uint64_t)d;
   fa::BwdParams p;
   const bool fp16 = dtype == FA_FP16;
   if (!encode_bnhd(&p.tm_q, q, B, H, N, d, fp16) || !encode_bnhd(&p.tm_k, k, B, H, N, d, fp16) ||

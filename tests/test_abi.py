@@ -140,3 +140,34 @@ def test_selftest_wait_timeout_host_checks(lib):
     import torch
     if not torch.cuda.is_available():
         assert lib.fa_selftest_wait_timeout(1000, None) in (FA_ERR_CUDA, FA_ERR_ARCH)
+
+
+def test_fwd_host_device_buffers_disjoint(lib):
+    # the host entry point writes q_d, k_d, v_d itself, so inputs may not share memory either
+    h = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000]
+    dvc = [0x10000, 0x10000 + 0x100, 0x30000, 0x40000, 0x50000]       # k_d over q_d
+    assert lib.fa_fwd_host(*h, *dvc, 2, 1, 128, 64, 0, 0.125, 0, None) == FA_ERR_ALIAS
+
+
+def test_bwd_host_host_side_checks(lib):
+    # Fake, never dereferenced addresses: every case below fails a host-side check first.
+    # B=2, H=1, N=128, d=64: 32 KiB per tensor, 65 KiB of workspace; buffers 1 MiB apart.
+    h = [0x1000 * (i + 1) for i in range(9)]
+    dvc = [0x100000 * (i + 1) for i in range(9)]
+    ws, ws_bytes = 0x100000 * 10, int(lib.fa_bwd_workspace_size(2, 1, 128, 64))
+
+    def call(hosts=h, devs=dvc, w=ws, wb=ws_bytes, B=2, N=128, d=64, dtype=0):
+        return lib.fa_bwd_host(*hosts, *devs, w, wb, B, 1, N, d, 0, 0.125, dtype, None)
+
+    assert call(hosts=h[:8] + [0]) == FA_ERR_NULL
+    assert call(hosts=[0] + h[1:]) == FA_ERR_NULL
+    assert call(devs=dvc[:4] + [0] + dvc[5:]) == FA_ERR_NULL
+    assert call(w=0) == FA_ERR_NULL
+    assert call(B=0) == FA_ERR_SHAPE
+    assert call(d=256) == FA_ERR_SHAPE
+    assert call(dtype=7) == FA_ERR_DTYPE
+    assert call(wb=ws_bytes - 4) == -11                                  # FA_ERR_WORKSPACE
+    assert call(devs=dvc[:6] + [dvc[6] + 8] + dvc[7:]) == FA_ERR_ALIGN   # dq_d
+    assert call(devs=dvc[:4] + [dvc[3] + 0x100] + dvc[5:]) == FA_ERR_ALIAS   # do_d over o_d
+    assert call(devs=dvc[:1] + [dvc[0] + 0x100] + dvc[2:]) == FA_ERR_ALIAS   # k_d over q_d
+    assert call(w=dvc[8] + 0x100) == FA_ERR_ALIAS                        # workspace over dv_d

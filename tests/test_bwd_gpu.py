@@ -117,3 +117,35 @@ def test_bwd_full_size_sampled(name, heads):
             err = np.linalg.norm(g - r) / np.linalg.norm(r)
             mx = np.abs(g - r).max() / np.abs(r).max()
             assert err <= REL_L2 and mx <= REL_MAX, (name, b, h, name_g, err, mx)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,pinned", [
+    (1, 4, 200, 64, True, True), (3, 4, 1000, 128, False, True),
+    (2, 16, 8192, 128, True, True),     # several head groups
+    (3, 11, 4096, 64, False, False)])   # uneven groups, pageable host memory
+def test_bwd_host_entry_matches_device_path(B, H, N, d, causal, pinned):
+    """fa_bwd_host (host buffers, head groups packed by pitched copies, copies overlapping the
+    kernels) gives the device path's gradients: dK and dV exactly (each is written once by one
+    CTA); dQ to within one rounding of the output type, since its fp32 partial sums arrive from
+    the key blocks' CTAs in no fixed order."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    qb, kb, vb = make_qkv(B, H, N, d, "bf16", seed=8500 + B + N)
+    dob = round_to_bits(normal((B, N, H, d), 8600 + N), "bf16")
+    host = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) for x in (qb, kb, vb, dob)]
+    dev = [t.cuda() for t in host]
+    o, lse = binding.attention_forward(*dev[:3], causal=causal)
+    ins = host[:3] + [o.cpu(), host[3], lse.cpu()]
+    if pinned:
+        ins = [t.pin_memory() for t in ins]
+    g_h = binding.attention_backward(*ins, causal=causal)
+    g_d = binding.attention_backward(*dev[:3], o, dev[3], lse, causal=causal)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    assert all(not t.is_cuda for t in g_h)
+    for name, a, b in zip(("dk", "dv"), g_h[1:], g_d[1:]):
+        assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16)), name
+    dq_h, dq_d = g_h[0].double(), g_d[0].cpu().double()
+    assert torch.isfinite(dq_h).all()
+    assert (dq_h - dq_d).abs().le(2.0 ** -7 * dq_d.abs() + 1e-6).all()
