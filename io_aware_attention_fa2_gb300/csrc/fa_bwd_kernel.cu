@@ -38,6 +38,8 @@
 // Warps: 0 TMA producer (K_j, V_j once; Q_i, dO_i into a 2-deep ring), 1 MMA issuer and TMEM
 // allocator, 2..5 softmax / dS (thread <-> TMEM lane), 6..9 dQ read-out and reduction.
 // Every wait is bounded.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -227,7 +229,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                   const float* __restrict__ dpre, float* __restrict__ dq_acc,
                   void* __restrict__ dk_ptr, void* __restrict__ dv_ptr, int H, int N, int causal,
-                  float scale, float scale_log2) {
+                  float scale, float scale_log2, int heads_per_group) {
   using L = BwdSmem<D>;
   static_assert(L::kDynamic <= 227 * 1024, "backward tiles exceed shared memory");
   extern __shared__ uint8_t smem_raw[];
@@ -242,11 +244,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto bar = [&](int i) { return smem_base + L::kBars + 8u * static_cast<uint32_t>(i); };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Unit: (b, h) x K/V block; blocks of one head are consecutive, longest (causal) first.
+  // Unit: (b, h) x K/V block. Heads go in groups of `heads_per_group` (sized on the host so
+  // that a group's Q, dO and dQ partial sums stay in L2); within a group, units go K/V block by
+  // K/V block across the group's heads, longest (causal) walk first, so that the long walks of
+  // the last group do not start at the end of the grid.
   const int num_kv = (N + BLOCK_N - 1) / BLOCK_N;
   const int num_q = (N + BLOCK_M - 1) / BLOCK_M;
-  const int bh = static_cast<int>(blockIdx.x) / num_kv;
-  const int jb = static_cast<int>(blockIdx.x) % num_kv;   // K/V block (block 0 sees most Q)
+  const int num_bh = static_cast<int>(gridDim.x) / num_kv;
+  const int group_units = heads_per_group * num_kv;
+  const int grp = static_cast<int>(blockIdx.x) / group_units;
+  const int rem = static_cast<int>(blockIdx.x) % group_units;
+  const int g_size = min(heads_per_group, num_bh - grp * heads_per_group);
+  const int bh = grp * heads_per_group + rem % g_size;
+  const int jb = rem / g_size;                              // K/V block (block 0 sees most Q)
   const int b = bh / H, h = bh % H;
   const int i0 = causal ? jb : 0;                          // first Q block that sees block jb
   const int steps = num_q - i0;
@@ -624,9 +634,15 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const long long num_kv = (p.N + BLOCK_N - 1) / BLOCK_N;
-  kernel<<<static_cast<unsigned>(num_kv * p.B * p.H), kBwdThreads, smem, stream>>>(
+  const long long bh = static_cast<long long>(p.B) * p.H;
+  // Heads per dispatch group: the group's Q and dO (2 bytes each) and dQ partial sums (4 bytes)
+  // within ~64 MiB of L2.
+  const long long bytes_per_head = 8ll * p.N * p.d;
+  const int heads_per_group =
+      static_cast<int>(std::max(1ll, std::min(bh, (64ll << 20) / bytes_per_head)));
+  kernel<<<static_cast<unsigned>(num_kv * bh), kBwdThreads, smem, stream>>>(
       p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.lse, p.dpre, p.dq_acc, p.dk, p.dv, p.H, p.N, p.causal,
-      p.scale, p.scale * kLog2e);
+      p.scale, p.scale * kLog2e, heads_per_group);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   fa_bwd_post_kernel<D, FP16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
