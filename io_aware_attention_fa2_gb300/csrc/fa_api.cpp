@@ -296,9 +296,9 @@ int check_backward(const void* q, const void* k, const void* v, const void* o,
 
 namespace {
 
-// Per device: the two copy streams of fa_fwd_host and its events, created on first use and
-// kept for the life of the process. One mutex serialises the enqueueing of fa_fwd_host calls,
-// so that two callers never interleave their event records and waits.
+// Per device: the two copy streams of fa_fwd_host / fa_bwd_host and their events, created on
+// first use and kept for the life of the process. One mutex serialises the enqueueing of the
+// host-buffer calls, so that two callers never interleave their event records and waits.
 struct HostPipe {
   cudaStream_t in = nullptr, out = nullptr;
   std::vector<cudaEvent_t> events;
@@ -321,10 +321,10 @@ int host_pipe(int device, size_t events, HostPipe** out) {
   return FA_OK;
 }
 
-constexpr int kHostChunks = 4;   // up to 2 * kHostChunks chunks per call
+constexpr int kMaxHostGroups = 8;   // head groups per host-buffer call, at most
 
 // Number of head groups a host-buffer call is cut into (the groups' copies overlap the kernels
-// of other groups). At most H and 2 * kHostChunks, each with at least 16 MB of copies (below
+// of other groups). At most H and kMaxHostGroups, each with at least 16 MB of copies (below
 // that, the per-group launch and copy set-up costs more than the overlap saves). When the
 // copies clearly dominate (kernel time estimated below half the copy time, at ~1 PFLOP/s
 // against ~200 GB/s over the host link), as many groups as allowed: the last group's kernel
@@ -339,7 +339,7 @@ int host_groups(int device, int H, long long units, double flops, double copy_by
     return FA_ERR_CUDA;
   const bool copy_bound = flops / 1e15 < 0.5 * copy_bytes / 200e9;
   const long long max_groups = std::max<long long>(
-      1, std::min<long long>({(long long)H, 2ll * kHostChunks,
+      1, std::min<long long>({(long long)H, (long long)kMaxHostGroups,
                               (long long)(copy_bytes / (16.0 * (1 << 20)))}));
   *groups = (int)std::max<long long>(
       1, copy_bound ? max_groups : std::min<long long>(max_groups, units / (2ll * sms)));
