@@ -71,6 +71,15 @@ def allowed_pairs(w) -> int:
     return total * w.H
 
 
+def metric_name(w, bwd: bool) -> str:
+    """The JSON line's metric; the same string on both arms for the same workload."""
+    if bwd:
+        return "attn bwd TFLOP/s (2.5x the forward's FLOPs)"
+    if w.name == DEFAULT_WORKLOAD:
+        return "attn fwd TFLOP/s (causal N=8K d=128 headline)"
+    return "attn fwd TFLOP/s"
+
+
 def metric_flops(w) -> float:
     """4*B*H*N^2*d (halved when causal) for Nq = Nk; with fewer queries than keys, 4*B*H*d per
     visible (query, key) pair (causal: query i sees i + Nk - Nq + 1 keys); with a padding or
@@ -285,7 +294,7 @@ def run_reference(args, w):
               "pro rata of the workload's metric FLOPs" % (n, s.total_rows,
                                                            100.0 * n / s.total_rows))
     line = {
-        "impl": "reference", "metric": "attn fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": metric_name(w, False), "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -530,9 +539,7 @@ def run_gpu(args, w):
         peak, peak_sus, hbm_peak, peak_src = measured_peaks()
         achieved = flops / (kernel_ms * 1e-3) / 1e12
         line = {
-            "metric": ("attn bwd TFLOP/s (2.5x the forward's FLOPs)" if bwd else
-                       "attn fwd TFLOP/s (causal N=8K d=128 headline)" if w.name ==
-                       DEFAULT_WORKLOAD else "attn fwd TFLOP/s"),
+            "metric": metric_name(w, bwd),
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
@@ -624,6 +631,8 @@ def main():
     if args.pass_ == "bwd" and (w.Nk or w.masked):
         ap.error("the backward takes one length N and the causal mask only")
     if args.impl == "reference":
+        if args.pass_ == "bwd":
+            ap.error("the reference arm times the forward oracle only")
         return run_reference(args, w)
     return run_gpu(args, w)
 

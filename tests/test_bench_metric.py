@@ -57,3 +57,15 @@ def test_masked_workloads_are_masked():
         assert w.masked and bench.metric_flops(w) < 4.0 * w.B * w.H * w.N * w.N * w.d
     w = dataclasses.replace(WORKLOADS["n8k_d128_padded"], B=2, N=64, seqlens_k=(64, 10))
     assert bench.allowed_pairs(w) == w.H * 64 * (64 + 10)
+
+
+def test_reference_arm_reports_the_gpu_arms_metric():
+    """Both arms of the bench print the same metric string for the same workload, so that their
+    lines can be paired; the headline workload carries its own label."""
+    import inspect
+    src = inspect.getsource(bench.run_reference) + inspect.getsource(bench.run_gpu)
+    assert src.count("metric_name(") == 2
+    names = {bench.metric_name(w, False) for w in WORKLOADS.values()}
+    assert bench.metric_name(WORKLOADS[bench.DEFAULT_WORKLOAD], False) in names
+    assert len(names) == 2
+    assert "bwd" in bench.metric_name(WORKLOADS[bench.DEFAULT_WORKLOAD], True)
