@@ -87,7 +87,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
                                          vp, dbl, vp, vp, vp]
     lib.oracle_attention_bwd.restype = i32
     lib.oracle_attention_bwd_sampled.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, i32,
-                                                 dbl, vp, i64, vp, i64, vp, i64, vp, vp, vp]
+                                                 i64, i64, vp, dbl, vp, i64, vp, i64, vp, i64,
+                                                 vp, vp, vp]
     lib.oracle_attention_bwd_sampled.restype = i32
     for fn in (lib.oracle_decode, lib.oracle_attention, lib.oracle_attention_rows,
                lib.oracle_attention_masked, lib.oracle_attention_rows_masked,
@@ -229,11 +230,13 @@ def attention_bwd(q, k, v, dout, causal: bool, scale: float, dtype: str | None =
 
 
 def attention_bwd_sampled(q, k, v, dout, causal: bool, scale: float, heads, keys, queries,
-                          dtype: str | None = None, lib: ctypes.CDLL | None = None):
+                          dtype: str | None = None, lib: ctypes.CDLL | None = None,
+                          window=(-1, -1), seqlens_k=None):
     """The gradients of ``attention_bwd`` on sampled outputs only, without N x N storage:
     for each (b, h) in ``heads``, dK and dV at the key positions ``keys`` and dQ at the query
     positions ``queries``. Returns float64 arrays dq [len(heads), len(queries), d] and dk, dv
-    [len(heads), len(keys), d]. Causal or no mask; queries and keys share N."""
+    [len(heads), len(keys), d]. The masks of ``attention`` (causal, window, key lengths);
+    queries and keys share N."""
     lib = lib or load()
     kind, (q, k, v) = _kind_and_arrays(q, k, v, dtype)
     _, (dout, _, _) = _kind_and_arrays(dout, dout, dout, dtype)
@@ -246,10 +249,12 @@ def attention_bwd_sampled(q, k, v, dout, causal: bool, scale: float, heads, keys
     dq = np.empty((len(hs), len(qs), d), dtype=np.float64)
     dk = np.empty((len(hs), len(ks), d), dtype=np.float64)
     dv = np.empty((len(hs), len(ks), d), dtype=np.float64)
+    lens, lens_ptr = _lengths(seqlens_k, B)
     rc = lib.oracle_attention_bwd_sampled(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), kind, B, H, Nq,
-                                          d, int(bool(causal)), float(scale), _ptr(hs), len(hs),
-                                          _ptr(ks), len(ks), _ptr(qs), len(qs), _ptr(dq),
-                                          _ptr(dk), _ptr(dv))
+                                          d, int(bool(causal)), int(window[0]), int(window[1]),
+                                          lens_ptr, float(scale), _ptr(hs), len(hs), _ptr(ks),
+                                          len(ks), _ptr(qs), len(qs), _ptr(dq), _ptr(dk),
+                                          _ptr(dv))
     if rc:
         raise RuntimeError("oracle_attention_bwd_sampled failed: %d" % rc)
     return dq, dk, dv

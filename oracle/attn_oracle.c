@@ -271,9 +271,11 @@ int oracle_attention_rows(const void* q, const void* k, const void* v, int kind,
  */
 int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, const void* dout,
                                  int kind, int64_t B, int64_t H, int64_t N, int64_t d,
-                                 int causal, double scale, const int64_t* heads, int64_t nheads,
-                                 const int64_t* keys, int64_t nkeys, const int64_t* queries,
-                                 int64_t nqueries, double* dq, double* dk, double* dv) {
+                                 int causal, int64_t window_left, int64_t window_right,
+                                 const int32_t* seqlens_k, double scale, const int64_t* heads,
+                                 int64_t nheads, const int64_t* keys, int64_t nkeys,
+                                 const int64_t* queries, int64_t nqueries, double* dq, double* dk,
+                                 double* dv) {
     int rc = check_args(q, k, v, kind, B, H, N, N, d);
     if (rc) return rc;
     if (!dout || !heads || nheads < 0 || nkeys < 0 || nqueries < 0) return -1;
@@ -294,20 +296,22 @@ int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, co
     }
     for (int64_t t = 0; t < nheads; ++t) {
         const int64_t b = heads[2 * t], h = heads[2 * t + 1];
+        const int64_t len_b = batch_key_length(seqlens_k, b, N);
 #define ROW(i) ((((b) * N + (i)) * H + (h)) * d)
-        /* 1. row statistics of every query of this head */
+        /* 1. row statistics of every query of this head, over its allowed keys [lo, hi) */
 #pragma omp parallel for schedule(dynamic, 16)
         for (int64_t i = 0; i < N; ++i) {
-            const int64_t hi = causal ? i + 1 : N;
+            int64_t lo, hi;
+            key_range(i, causal, window_left, window_right, len_b, &lo, &hi);
             double mi = -INFINITY;
-            for (int64_t j = 0; j < hi; ++j) {
+            for (int64_t j = lo; j < hi; ++j) {
                 double dot = 0.0;
                 for (int64_t c = 0; c < d; ++c)
                     dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
                 if (scale * dot > mi) mi = scale * dot;
             }
             double li = 0.0, di = 0.0;
-            for (int64_t j = 0; j < hi; ++j) {
+            for (int64_t j = lo; j < hi; ++j) {
                 double dot = 0.0, dp = 0.0;
                 for (int64_t c = 0; c < d; ++c) {
                     dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
@@ -319,16 +323,19 @@ int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, co
             }
             m[i] = mi;
             l[i] = li;
-            D[i] = di / li;
+            D[i] = li > 0.0 ? di / li : 0.0;
         }
-        /* 2. dV_j, dK_j for the sampled keys */
+        /* 2. dV_j, dK_j for the sampled keys: every query whose allowed range holds key j */
 #pragma omp parallel for schedule(dynamic, 1)
         for (int64_t u = 0; u < nkeys; ++u) {
             const int64_t j = keys[u];
             double* gk = dk + (t * nkeys + u) * d;
             double* gv = dv + (t * nkeys + u) * d;
             for (int64_t c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
-            for (int64_t i = causal ? j : 0; i < N; ++i) {
+            for (int64_t i = 0; i < N; ++i) {
+                int64_t lo, hi;
+                key_range(i, causal, window_left, window_right, len_b, &lo, &hi);
+                if (j < lo || j >= hi) continue;
                 double dot = 0.0, dp = 0.0;
                 for (int64_t c = 0; c < d; ++c) {
                     dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
@@ -343,13 +350,15 @@ int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, co
             }
             for (int64_t c = 0; c < d; ++c) gk[c] *= scale;
         }
-        /* 3. dQ_i for the sampled queries */
+        /* 3. dQ_i for the sampled queries, over their allowed keys */
 #pragma omp parallel for schedule(dynamic, 1)
         for (int64_t u = 0; u < nqueries; ++u) {
             const int64_t i = queries[u];
             double* gq = dq + (t * nqueries + u) * d;
             for (int64_t c = 0; c < d; ++c) gq[c] = 0.0;
-            for (int64_t j = 0; j < (causal ? i + 1 : N); ++j) {
+            int64_t lo, hi;
+            key_range(i, causal, window_left, window_right, len_b, &lo, &hi);
+            for (int64_t j = lo; j < hi; ++j) {
                 double dot = 0.0, dp = 0.0;
                 for (int64_t c = 0; c < d; ++c) {
                     dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);

@@ -531,22 +531,27 @@ def pin_bwd_matches_torch_autograd(lib):
 
 def pin_bwd_sampled_matches_full(lib):
     """The sampled backward (no N x N storage, used at full sizes) equals the full backward's
-    gradients at the sampled positions, for both masks, on real and on bf16 inputs."""
+    gradients at the sampled positions, causal or not, with and without a window and key
+    lengths (one batch with no key at all), on real and on bf16 inputs."""
     from io_aware_attention_fa2_gb300.inputs import round_to_bits
     rng = _rng(33)
     B, N, H, d = 2, 41, 3, 8
     real = [rng.standard_normal((B, N, H, d)) for _ in range(4)]
-    heads, keys, queries = [(0, 0), (1, 2), (0, 1)], [0, 1, 20, 39, 40], [0, 2, 21, 40]
+    heads, keys, queries = [(0, 0), (1, 2), (0, 1)], [0, 1, 20, 29, 39, 40], [0, 2, 21, 40]
+    masks = [((-1, -1), None), ((5, 3), None), ((-1, -1), [30, 41]), ((6, 0), [41, 0])]
     for dtype in (None, "bf16"):
         args = real if dtype is None else [round_to_bits(x, "bf16") for x in real]
         for causal in (False, True):
-            dq, dk, dv = oracle.attention_bwd(*args, causal, 0.37, dtype=dtype, lib=lib)
-            sq, sk, sv = oracle.attention_bwd_sampled(*args, causal, 0.37, heads, keys, queries,
-                                                      dtype=dtype, lib=lib)
-            for t, (b, h) in enumerate(heads):
-                assert np.abs(sq[t] - dq[b, queries, h]).max() < 1e-12
-                assert np.abs(sk[t] - dk[b, keys, h]).max() < 1e-12
-                assert np.abs(sv[t] - dv[b, keys, h]).max() < 1e-12
+            for window, lens in masks:
+                dq, dk, dv = oracle.attention_bwd(*args, causal, 0.37, dtype=dtype, lib=lib,
+                                                  window=window, seqlens_k=lens)
+                sq, sk, sv = oracle.attention_bwd_sampled(
+                    *args, causal, 0.37, heads, keys, queries, dtype=dtype, lib=lib,
+                    window=window, seqlens_k=lens)
+                for t, (b, h) in enumerate(heads):
+                    assert np.abs(sq[t] - dq[b, queries, h]).max() < 1e-12
+                    assert np.abs(sk[t] - dk[b, keys, h]).max() < 1e-12
+                    assert np.abs(sv[t] - dv[b, keys, h]).max() < 1e-12
 
 
 ALL_PINS += [pin_bwd_finite_differences, pin_bwd_identities, pin_bwd_matches_torch_autograd,

@@ -59,8 +59,10 @@ MUTANTS = [
     ("bwd_dk_transposed", "const double ds = dS[i * N + j], p = P[i * N + j];",
      "const double ds = dS[j * N + i], p = P[i * N + j];"),
     ("bwd_sampled_drops_D", "const double ds = p * (dp - D[i]);", "const double ds = p * dp;"),
-    ("bwd_sampled_causal_off_by_one", "for (int64_t i = causal ? j : 0; i < N; ++i) {",
-     "for (int64_t i = causal ? j + 1 : 0; i < N; ++i) {"),
+    ("bwd_sampled_key_left_bound_ignored", "if (j < lo || j >= hi) continue;",
+     "if (j >= hi) continue;"),
+    ("bwd_sampled_key_right_bound_off_by_one", "if (j < lo || j >= hi) continue;",
+     "if (j < lo || j > hi) continue;"),
 ]
 
 
