@@ -447,7 +447,7 @@ def run_gpu(args, w):
 
         def step():
             binding.fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, w.causal, w.scale, bwd_ws,
-                           stream)
+                           stream, w.window, lens_dev)
 
         if rank == 0 and not args.no_check:
             # parity of dQ, dK, dV on sampled positions of one head against the fp64 oracle
@@ -459,8 +459,9 @@ def run_gpu(args, w):
             pos = np.unique(np.concatenate([
                 [0, 1, 127, 128, w.N // 2, w.N - 1],
                 np.random.default_rng(w.seed + 6).integers(0, w.N, 6)]))
-            sq, sk, sv = oracle.attention_bwd_sampled(qb, kb, vb, dob, w.causal, w.scale,
-                                                      [(b0, h0)], pos, pos, dtype=w.dtype)
+            sq, sk, sv = oracle.attention_bwd_sampled(
+                qb, kb, vb, dob, w.causal, w.scale, [(b0, h0)], pos, pos, dtype=w.dtype,
+                window=w.window, seqlens_k=list(w.seqlens_k) if w.seqlens_k else None)
             sel = torch.from_numpy(pos).to(dev)
             got = [t[b0, sel, h0].double().cpu().numpy() for t in (dq, dk, dv)]
             parity = {"head": [int(b0), int(h0)], "positions": int(len(pos))}
@@ -516,7 +517,8 @@ def run_gpu(args, w):
 
         def e2e_step():
             binding.attention_backward(*host[:3], o_pin, host[3], l_pin, causal=w.causal,
-                                       scale=w.scale, stream=stream, device=dev)
+                                       scale=w.scale, stream=stream, device=dev,
+                                       window=w.window, seqlens_k=lens_host)
 
     for _ in range(max(1, args.warmup // 2)):
         e2e_step()
@@ -628,8 +630,8 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
-    if args.pass_ == "bwd" and (w.Nk or w.masked):
-        ap.error("the backward takes one length N and the causal mask only")
+    if args.pass_ == "bwd" and w.Nk:
+        ap.error("the backward takes one length N (queries and keys)")
     if args.impl == "reference":
         if args.pass_ == "bwd":
             ap.error("the reference arm times the forward oracle only")

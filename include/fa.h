@@ -201,7 +201,7 @@ int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, fl
  *   dout         [B, N, H, d] dtype: the gradient of the loss with respect to o
  *   lse          [B, H, N] fp32: the forward's LSE for the same q, k, v, causal and scale
  *   dq, dk, dv   [B, N, H, d] dtype, written (every element)
- *   causal, scale, dtype, d: as in fa_fwd (no window or key-length masks here)
+ *   causal, scale, dtype, d: as in fa_fwd (window and key-length masks: fa_bwd_masked)
  *   workspace    device memory of at least fa_bwd_workspace_size(B, H, N, d) bytes, 16-byte
  *                aligned, owned by the caller, not overlapping any other argument: fp32 dQ
  *                partial sums and D. Calls sharing a workspace must not overlap.
@@ -213,6 +213,21 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
            int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
            fa_stream_t stream);
+
+/*
+ * fa_bwd_masked -- fa_bwd for the attention fa_fwd_masked computes with Nq = Nk = N: the same
+ * window (window_left, window_right; negative = no bound) and per-batch key lengths (seqlens_k:
+ * device int32 [B], 4-byte aligned, or NULL), on top of `causal`. The gradients are those of
+ * that masked attention: a key no query sees gets dK = dV = 0, a query that sees no key gets
+ * dQ = 0 (its forward LSE is -inf). `lse` must come from fa_fwd_masked with the same masks.
+ * Every other argument, the workspace and the return codes as in fa_bwd (seqlens_k must not
+ * overlap an output).
+ */
+int fa_bwd_masked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  int causal, int window_left, int window_right, const int* seqlens_k,
+                  float scale, int dtype, void* workspace, size_t workspace_bytes,
+                  fa_stream_t stream);
 
 /* Bytes of workspace fa_bwd needs: B*H*N*(d + 1)*4. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);

@@ -62,6 +62,9 @@ def load_library() -> ctypes.CDLL:
             lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                    f32, i32, vp, ctypes.c_size_t, vp]
             lib.fa_bwd.restype = i32
+            lib.fa_bwd_masked.argtypes = [vp] * 9 + [i32] * 7 + [vp, f32, i32, vp,
+                                                                 ctypes.c_size_t, vp]
+            lib.fa_bwd_masked.restype = i32
             lib.fa_fwd_host.argtypes = [vp] * 10 + [i32, i32, i32, i32, i32, f32, i32, vp]
             lib.fa_fwd_host.restype = i32
             lib.fa_bwd_host.argtypes = [vp] * 19 + [ctypes.c_size_t] + [i32] * 5 + [f32, i32,
@@ -221,10 +224,12 @@ def bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
 
 
 def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool, scale: float, workspace=None,
-           stream=None) -> None:
+           stream=None, window=(-1, -1), seqlens_k=None) -> None:
     """Enqueue the backward: dq, dk, dv [B, N, H, d] from the forward's q, k, v, o, lse and
     the upstream gradient dout. ``workspace``: a CUDA tensor of at least bwd_workspace_size
-    bytes, or None to let PyTorch allocate one."""
+    bytes, or None to let PyTorch allocate one. ``window`` and ``seqlens_k`` (int32 CUDA
+    tensor [B]) select the masks of fa_fwd_masked; lse must come from the forward with the
+    same masks."""
     import torch
     B, N, H, d = q.shape
     for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk),
@@ -236,13 +241,20 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal: bool, scale: float, worksp
     need = bwd_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    rc = load_library().fa_bwd(
+    lens_ptr = None
+    if seqlens_k is not None:
+        if (not seqlens_k.is_cuda or seqlens_k.dtype != torch.int32
+                or tuple(seqlens_k.shape) != (B,) or not seqlens_k.is_contiguous()):
+            raise ValueError("seqlens_k must be a contiguous int32 CUDA tensor [B]")
+        lens_ptr = seqlens_k.data_ptr()
+    left, right = (int(w) for w in window)
+    rc = load_library().fa_bwd_masked(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
-        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
-        _dtype_code(q), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-        _stream_handle(stream))
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, int(bool(causal)), left, right,
+        lens_ptr, float(scale), _dtype_code(q), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc != FA_OK:
-        raise FaError(rc, "fa_bwd")
+        raise FaError(rc, "fa_bwd_masked")
 
 
 def device_error(stream=None) -> int:
@@ -323,8 +335,9 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
 
 
 def attention_backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
-                       stream=None, device=None):
-    """dq, dk, dv = gradients of sum(dout * o) for o, lse = attention_forward(q, k, v, causal).
+                       stream=None, device=None, window=(-1, -1), seqlens_k=None):
+    """dq, dk, dv = gradients of sum(dout * o) for o, lse = attention_forward(q, k, v, causal,
+    window=window, seqlens_k=seqlens_k) (queries and keys share N).
 
     Device tensors are used in place; host tensors (ideally pinned) are copied to ``device``
     (default cuda:0), the kernels run there, and the gradients come back as host tensors.
@@ -335,9 +348,11 @@ def attention_backward(q, k, v, o, dout, lse, causal: bool = False, scale: float
     B, N, H, d = q.shape
     if scale is None:
         scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+    masked = seqlens_k is not None or tuple(window) != (-1, -1)
     if q.is_cuda:
         dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-        fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal, scale, None, stream)
+        lens = None if seqlens_k is None else seqlens_k.to(q.device, torch.int32)
+        fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal, scale, None, stream, window, lens)
         return dq, dk, dv
     for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout)):
         if t.shape != q.shape or t.dtype != q.dtype or t.is_cuda or not t.is_contiguous():
@@ -349,6 +364,18 @@ def attention_backward(q, k, v, o, dout, lse, causal: bool = False, scale: float
     dev = torch.device(device or "cuda:0")
     st = stream if stream is not None else torch.cuda.current_stream(dev)
     host = [torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned()) for _ in range(3)]
+    if masked:
+        # masks: copies in, fa_bwd_masked, copies out, all on `st`
+        with torch.cuda.stream(st):
+            dev_in = [t.to(dev, non_blocking=True) for t in (q, k, v, o, dout, lse)]
+            grads = [torch.empty_like(dev_in[0]) for _ in range(3)]
+            lens = (None if seqlens_k is None
+                    else seqlens_k.to(dev, torch.int32, non_blocking=True))
+            fa_bwd(*dev_in, *grads, causal, scale, None, st, window, lens)
+            for h_, g_ in zip(host, grads):
+                h_.copy_(g_, non_blocking=True)
+        st.synchronize()
+        return tuple(host)
     with torch.cuda.device(dev):
         bufs = [torch.empty(q.shape, dtype=q.dtype, device=dev) for _ in range(8)]
         ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)

@@ -256,7 +256,8 @@ namespace {
 int check_backward(const void* q, const void* k, const void* v, const void* o,
                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
                    int H, int N, int d, float scale, int dtype, void* workspace,
-                   size_t workspace_bytes, bool inputs_written = false) {
+                   size_t workspace_bytes, bool inputs_written = false,
+                   const int* seqlens_k = nullptr) {
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
     return FA_ERR_NULL;
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return FA_ERR_SHAPE;
@@ -273,14 +274,15 @@ int check_backward(const void* q, const void* k, const void* v, const void* o,
                         static_cast<const void*>(workspace)})
     if (reinterpret_cast<uintptr_t>(p) % 16) return FA_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(lse) % 4) return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(seqlens_k) % 4) return FA_ERR_ALIGN;
   struct Span { const void* p; uint64_t n; };
   const Span ins[] = {{q, t_bytes}, {k, t_bytes}, {v, t_bytes}, {o, t_bytes}, {dout, t_bytes},
-                      {lse, lse_bytes}};
+                      {lse, lse_bytes}, {seqlens_k, seqlens_k ? (uint64_t)B * 4 : 0}};
   const Span outs[] = {{dq, t_bytes}, {dk, t_bytes}, {dv, t_bytes},
                        {workspace, fa_bwd_workspace_size(B, H, N, d)}};
   for (const Span& out : outs)
     for (const Span& in : ins)
-      if (overlaps(out.p, out.n, in.p, in.n)) return FA_ERR_ALIAS;
+      if (in.p && overlaps(out.p, out.n, in.p, in.n)) return FA_ERR_ALIAS;
   for (int i = 0; i < 4; ++i)
     for (int j = i + 1; j < 4; ++j)
       if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return FA_ERR_ALIAS;
@@ -522,12 +524,13 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 
 extern "C" {
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-           int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
-           fa_stream_t stream) {
+int fa_bwd_masked(const void* q, const void* k, const void* v, const void* o,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H,
+                  int N, int d, int causal, int window_left, int window_right,
+                  const int* seqlens_k, float scale, int dtype, void* workspace,
+                  size_t workspace_bytes, fa_stream_t stream) {
   const int rc = check_backward(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, dtype,
-                                workspace, workspace_bytes);
+                                workspace, workspace_bytes, false, seqlens_k);
   if (rc != FA_OK) return rc;
   const uint64_t elems = (uint64_t)B * (uint64_t)H * (uint64_t)N * (uint64_t)d;
   fa::BwdParams p;
@@ -549,11 +552,24 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   p.N = N;
   p.d = d;
   p.causal = causal ? 1 : 0;
+  // a bound wider than the sequence is no narrower than none, and keeps the kernel's index
+  // arithmetic within int
+  p.window_left = window_left < 0 ? -1 : std::min(window_left, N);
+  p.window_right = window_right < 0 ? -1 : std::min(window_right, N);
+  p.seqlens_k = seqlens_k;
   p.fp16 = fp16 ? 1 : 0;
   p.scale = scale;
   if (fa::launch_bwd(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FA_ERR_LAUNCH;
   return FA_OK;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+           fa_stream_t stream) {
+  return fa_bwd_masked(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, -1, -1, nullptr,
+                       scale, dtype, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -176,11 +176,13 @@ __global__ void __launch_bounds__(256)
 
 // ---------------------------------------------------------------------------------------------
 // P^T for 32 queries of this thread's key, packed to 16-bit pairs: 2^(S^T scale log2e -
-// LSE log2e). l2 holds the 32 queries' LSE log2e (+inf for rows to ignore). MASKED: the first
-// `lim` queries of the chunk do not see the key (causal diagonal, keys past N).
+// LSE log2e). l2 holds the 32 queries' LSE log2e (+inf for rows to ignore). MASKED: only the
+// queries t of the chunk with lo <= t <= hi see the key (causal diagonal, window, keys past N or
+// past the batch's key length).
 template <bool MASKED, bool FP16>
 __device__ __forceinline__ void p_chunk(const uint32_t (&sr)[32], const float* __restrict__ l2,
-                                        float scale_log2, int lim, uint32_t* __restrict__ out) {
+                                        float scale_log2, int lo, int hi,
+                                        uint32_t* __restrict__ out) {
 #pragma unroll
   for (int t4 = 0; t4 < 8; ++t4) {
     const float4 l = reinterpret_cast<const float4*>(l2)[t4];
@@ -190,10 +192,10 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sr)[32], const float* _
     ptx::fma2(x2, x3, __uint_as_float(sr[4 * t4 + 2]), __uint_as_float(sr[4 * t4 + 3]),
               scale_log2, scale_log2, -l.z, -l.w);
     if constexpr (MASKED) {
-      if (4 * t4 < lim) x0 = -INFINITY;
-      if (4 * t4 + 1 < lim) x1 = -INFINITY;
-      if (4 * t4 + 2 < lim) x2 = -INFINITY;
-      if (4 * t4 + 3 < lim) x3 = -INFINITY;
+      if (4 * t4 < lo || 4 * t4 > hi) x0 = -INFINITY;
+      if (4 * t4 + 1 < lo || 4 * t4 + 1 > hi) x1 = -INFINITY;
+      if (4 * t4 + 2 < lo || 4 * t4 + 2 > hi) x2 = -INFINITY;
+      if (4 * t4 + 3 < lo || 4 * t4 + 3 > hi) x3 = -INFINITY;
     }
     out[2 * t4] = pack2<FP16>(ptx::exp2_approx(x0), ptx::exp2_approx(x1));
     out[2 * t4 + 1] = pack2<FP16>(ptx::exp2_approx(x2), ptx::exp2_approx(x3));
@@ -229,6 +231,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                   const float* __restrict__ dpre, float* __restrict__ dq_acc,
                   void* __restrict__ dk_ptr, void* __restrict__ dv_ptr, int H, int N, int causal,
+                  int window_left, int window_right, const int* __restrict__ seqlens_k,
                   float scale, float scale_log2, int heads_per_group) {
   using L = BwdSmem<D>;
   static_assert(L::kDynamic <= 227 * 1024, "backward tiles exceed shared memory");
@@ -258,8 +261,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int bh = grp * heads_per_group + rem % g_size;
   const int jb = rem / g_size;                              // K/V block (block 0 sees most Q)
   const int b = bh / H, h = bh % H;
-  const int i0 = causal ? jb : 0;                          // first Q block that sees block jb
-  const int steps = num_q - i0;
+  // Q blocks [i0, i0 + steps) hold a query that sees a key of this block: key j is visible to
+  // query i when j < the batch's key length, j <= i (causal), j >= i - window_left and
+  // j <= i + window_right (negative: no bound). Window bounds arrive clamped to [-1, N].
+  const int len = seqlens_k ? min(max(seqlens_k[b], 0), N) : N;
+  const int k0 = jb * BLOCK_N;
+  int i0 = causal ? k0 / BLOCK_M : 0;
+  if (window_right >= 0) i0 = max(i0, max(k0 - window_right, 0) / BLOCK_M);
+  int i_end = num_q;
+  if (window_left >= 0) i_end = min(i_end, (k0 + BLOCK_N - 1 + window_left) / BLOCK_M + 1);
+  if (k0 >= len) i_end = i0;
+  const int steps = max(i_end - i0, 0);
+  if (steps == 0) {
+    // No query sees a key of this block: dK = dV = 0 for its keys, nothing else to do.
+    if (warp >= 2 && warp < 6) {
+      const int key = k0 + (warp & 3) * 32 + lane;
+      if (key < N) {
+        for (int which = 0; which < 2; ++which) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(which ? dk_ptr : dv_ptr) +
+                                                ((static_cast<int64_t>(b) * N + key) * H + h) * D);
+#pragma unroll
+          for (int t = 0; t < D / 8; ++t) dst[t] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -433,7 +460,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int key = jb * BLOCK_N + r;
-    const bool key_ok = key < N;
+    const bool key_ok = key < len;   // keys past N or past the batch's key length see no query
+    // queries [q_lo, q_hi] see this key
+    int q_lo = causal ? key : 0, q_hi = N - 1;
+    if (window_right >= 0) q_lo = max(q_lo, key - window_right);
+    if (window_left >= 0) q_hi = min(q_hi, key + window_left);
     uint8_t* const ds_gen = smem_gen + L::kdS;
     float* const s_lse = stat;         // LSE_i * log2e, +inf for rows to ignore
     float* const s_d = stat + 128;     // D_i
@@ -468,7 +499,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // only if key <= q0 + t (causal); keys past N do not exist.
       if (!wait_w(BB_S_FULL, n & 1)) { ok = false; break; }
       ptx::tc_fence_after_sync();
-      const int lim = !key_ok ? BLOCK_M : (causal ? min(max(key - q0, 0), BLOCK_M) : 0);
+      // this step's query range of the key, relative to the block (empty when !key_ok)
+      const int lo = key_ok ? q_lo - q0 : BLOCK_M, hi = key_ok ? q_hi - q0 : -1;
       // P^T stays in TMEM (over the first 64 columns of S^T) until dS(i) has read it back.
 #pragma unroll 1
       for (int c = 0; c < BLOCK_M / 32; ++c) {
@@ -477,10 +509,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::tmem_wait_ld();
         ptx::reg_fence(sr);
         uint32_t pr[16];
-        if (lim > 32 * c)
-          p_chunk<true, FP16>(sr, s_lse + 32 * c, scale_log2, lim - 32 * c, pr);
+        if (lo > 32 * c || hi < 32 * c + 31)
+          p_chunk<true, FP16>(sr, s_lse + 32 * c, scale_log2, lo - 32 * c, hi - 32 * c, pr);
         else
-          p_chunk<false, FP16>(sr, s_lse + 32 * c, scale_log2, 0, pr);
+          p_chunk<false, FP16>(sr, s_lse + 32 * c, scale_log2, 0, 31, pr);
         ptx::tmem_st_32x32b_x16(tmem + lane_off + kT_S + c * 16, pr);
       }
       ptx::tmem_wait_st();
@@ -530,7 +562,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dV + which * D + c * 32, gr);
           ptx::tmem_wait_ld();
           ptx::reg_fence(gr);
-          if (key_ok) {
+          if (key < N) {
             uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
@@ -642,7 +674,7 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
       static_cast<int>(std::max(1ll, std::min(bh, (64ll << 20) / bytes_per_head)));
   kernel<<<static_cast<unsigned>(num_kv * bh), kBwdThreads, smem, stream>>>(
       p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.lse, p.dpre, p.dq_acc, p.dk, p.dv, p.H, p.N, p.causal,
-      p.scale, p.scale * kLog2e, heads_per_group);
+      p.window_left, p.window_right, p.seqlens_k, p.scale, p.scale * kLog2e, heads_per_group);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   fa_bwd_post_kernel<D, FP16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(

@@ -58,6 +58,9 @@ struct BwdParams {
   float* dpre;          // workspace: fp32 [B, H, N], D = rowsum(dO * O)
   int B, H, N, d;
   int causal;
+  int window_left;      // as in FwdParams (queries and keys share positions here)
+  int window_right;
+  const int* seqlens_k; // device int32 [B] or null, as in FwdParams
   int fp16;
   float scale;
 };

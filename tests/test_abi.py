@@ -171,3 +171,19 @@ def test_bwd_host_host_side_checks(lib):
     assert call(devs=dvc[:4] + [dvc[3] + 0x100] + dvc[5:]) == FA_ERR_ALIAS   # do_d over o_d
     assert call(devs=dvc[:1] + [dvc[0] + 0x100] + dvc[2:]) == FA_ERR_ALIAS   # k_d over q_d
     assert call(w=dvc[8] + 0x100) == FA_ERR_ALIAS                        # workspace over dv_d
+
+
+def test_bwd_masked_host_side_checks(lib):
+    # Fake, never dereferenced addresses; B=2, H=1, N=128, d=64: 32 KiB per tensor.
+    ptrs = [0x100000 * (i + 1) for i in range(9)]
+    ws, ws_bytes = 0x100000 * 10, int(lib.fa_bwd_workspace_size(2, 1, 128, 64))
+
+    def call(lens=0, left=-1, right=-1):
+        return lib.fa_bwd_masked(*ptrs, 2, 1, 128, 64, 1, left, right, lens, 0.125, 0, ws,
+                                 ws_bytes, None)
+
+    assert call(lens=0x2000002) == FA_ERR_ALIGN                 # key lengths not 4-byte aligned
+    assert call(lens=ptrs[6] + 64) == FA_ERR_ALIAS              # key lengths inside dq
+    # the unmasked call reaches the same checks as the masked one with no mask
+    assert lib.fa_bwd(*ptrs, 2, 1, 0, 64, 0, 0.125, 0, ws, ws_bytes, None) == FA_ERR_SHAPE
+    assert call(left=5, right=7) == call(left=-1, right=-1)     # only device checks remain

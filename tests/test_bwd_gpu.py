@@ -149,3 +149,124 @@ def test_bwd_host_entry_matches_device_path(B, H, N, d, causal, pinned):
     dq_h, dq_d = g_h[0].double(), g_d[0].cpu().double()
     assert torch.isfinite(dq_h).all()
     assert (dq_h - dq_d).abs().le(2.0 ** -7 * dq_d.abs() + 1e-6).all()
+
+
+def run_masked_case(B, H, N, d, causal, window, lens, seed):
+    """fa_fwd / fa_bwd with the window and key-length masks against the oracle's gradients of
+    the same masked attention."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    qb, kb, vb = make_qkv(B, H, N, d, "bf16", seed)
+    dob = round_to_bits(normal((B, N, H, d), seed + 9), "bf16")
+    q, k, v, do = (to_device(x, "bf16") for x in (qb, kb, vb, dob))
+    scale = softmax_scale(d)
+    lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device="cuda")
+    binding.fa_fwd(q, k, v, o, lse, causal, scale, None, window, lens_t)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    binding.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, scale, None, None, window, lens_t)
+    assert binding.device_error() == 0
+    got = [t.double().cpu().numpy() for t in (dq, dk, dv)]
+    ref = oracle.attention_bwd(qb, kb, vb, dob, causal, scale, dtype="bf16", window=window,
+                               seqlens_k=lens)
+    what = (B, H, N, d, causal, window, lens)
+    # keys past a batch's key length have no query, and a batch with no key has no gradient
+    # at all: exactly zero on the GPU as well
+    for b, n in enumerate(lens or []):
+        assert not got[1][b, n:].any() and not got[2][b, n:].any(), what
+        if n == 0:
+            assert not got[0][b].any(), what
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert np.isfinite(g).all(), (name, what)
+        if np.abs(r).max() < 1e-6:
+            assert np.abs(g).max() <= 1e-3, (name, what, float(np.abs(g).max()))
+            continue
+        err = np.linalg.norm(g - r) / np.linalg.norm(r)
+        mx = np.abs(g - r).max() / np.abs(r).max()
+        assert err <= REL_L2 and mx <= REL_MAX, (name, what, err, mx)
+
+
+MASKS = [((64, 0), None), ((100, 30), None), ((0, 0), None), ((-1, -1), "third"),
+         ((50, -1), "half_and_empty"), ((300, 200), "ragged")]
+
+
+@pytest.mark.parametrize("N", [200, 513])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("window,lens", MASKS, ids=[str(m) for m in MASKS])
+def test_bwd_masks(N, d, causal, window, lens):
+    """Sliding windows (one-sided, two-sided, the diagonal alone), key lengths (one batch with
+    no key at all, lengths that are not tile multiples), with and without causal."""
+    lens = {None: None, "third": [N, N // 3], "half_and_empty": [N // 2, 0],
+            "ragged": [N - 1, 129]}[lens]
+    run_masked_case(2, 2, N, d, causal, window, lens, seed=9900 + N + d)
+
+
+@pytest.mark.parametrize("name,heads", [("n8k_d128_window1k", [(0, 5), (1, 14)]),
+                                        ("n8k_d128_padded", [(0, 2), (1, 9)])])
+def test_bwd_masked_full_size_sampled(name, heads):
+    """The masked workloads at full size (B=2, H=16, N=8192, d=128 bf16: a causal 1024-key
+    window; key lengths 8192 and 5000), one fa_bwd call with the bench's upstream gradient;
+    sampled positions (tile edges, the window edge, the key-length edge, the last row) against
+    the sampled oracle with the same masks."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    w = WORKLOADS[name]
+    qb, kb, vb = make_workload(w)
+    dob = round_to_bits(normal(qb.shape, w.seed + 9), w.dtype)
+    q, k, v, do = (to_device(x, w.dtype) for x in (qb, kb, vb, dob))
+    lens = list(w.seqlens_k) if w.seqlens_k else None
+    lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, device="cuda")
+    binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale, None, w.window, lens_t)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    binding.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, None, None, w.window,
+                   lens_t)
+    assert binding.device_error() == 0
+    pos = np.unique(np.concatenate([[0, 1, 127, 128, 1023, 1024, 1025, 4999, 5000, 5001,
+                                     w.N // 2, w.N - 1],
+                                    np.random.default_rng(w.seed + 17).integers(0, w.N, 8)]))
+    ref = oracle.attention_bwd_sampled(qb, kb, vb, dob, w.causal, w.scale, heads, pos, pos,
+                                       dtype=w.dtype, window=w.window, seqlens_k=lens)
+    sel = torch.from_numpy(pos).cuda()
+    for t, (b, h) in enumerate(heads):
+        for name_g, g_all, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            g = g_all[b, sel, h].double().cpu().numpy()
+            r = r[t]
+            assert np.isfinite(g).all(), name_g
+            if lens and name_g != "dq":
+                assert not g[pos >= lens[b]].any(), (name, b, h, name_g)
+            err = np.linalg.norm(g - r) / np.linalg.norm(r)
+            mx = np.abs(g - r).max() / np.abs(r).max()
+            assert err <= REL_L2 and mx <= REL_MAX, (name, b, h, name_g, err, mx)
+
+
+def test_bwd_masked_host_path_matches_device_path():
+    """attention_backward with host tensors and masks (copies, fa_bwd_masked, copies back)
+    gives the device path's gradients."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    B, H, N, d = 2, 3, 700, 128
+    qb, kb, vb = make_qkv(B, H, N, d, "bf16", seed=9950)
+    dob = round_to_bits(normal((B, N, H, d), 9951), "bf16")
+    host = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) for x in (qb, kb, vb, dob)]
+    dev = [t.cuda() for t in host]
+    window, lens = (200, 0), [700, 333]
+    lens_t = torch.tensor(lens, dtype=torch.int32)
+    o, lse = binding.attention_forward(*dev[:3], causal=True, window=window,
+                                       seqlens_k=lens_t.cuda())
+    g_d = binding.attention_backward(*dev[:3], o, dev[3], lse, causal=True, window=window,
+                                     seqlens_k=lens_t.cuda())
+    g_h = binding.attention_backward(*host[:3], o.cpu(), host[3], lse.cpu(), causal=True,
+                                     window=window, seqlens_k=lens_t)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    for a, b in zip(g_h[1:], g_d[1:]):
+        assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
+    da, db = g_h[0].double(), g_d[0].cpu().double()
+    assert bool((da - db).abs().le(2.0 ** -7 * db.abs() + 1e-6).all())
