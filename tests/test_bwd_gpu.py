@@ -270,3 +270,62 @@ def test_bwd_masked_host_path_matches_device_path():
         assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
     da, db = g_h[0].double(), g_d[0].cpu().double()
     assert bool((da - db).abs().le(2.0 ** -7 * db.abs() + 1e-6).all())
+
+
+def test_bwd_partial_dispatch_group():
+    """B=1, H=11, N=8192, d=128: the backward's dispatch groups hold 8 heads (their Q, dO and dQ
+    partial sums within 64 MiB of L2), so the last group has 3; heads of both groups checked on
+    sampled positions against the sampled oracle."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    B, H, N, d = 1, 11, 8192, 128
+    qb, kb, vb = make_qkv(B, H, N, d, "bf16", seed=9960)
+    dob = round_to_bits(normal((B, N, H, d), 9961), "bf16")
+    q, k, v, do = (to_device(x, "bf16") for x in (qb, kb, vb, dob))
+    scale = softmax_scale(d)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device="cuda")
+    binding.fa_fwd(q, k, v, o, lse, True, scale)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    binding.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, True, scale)
+    assert binding.device_error() == 0
+    heads = [(0, 0), (0, 7), (0, 8), (0, 10)]
+    pos = np.array([0, 1, 127, 128, 4095, 4096, 8063, 8064, 8191])
+    ref = oracle.attention_bwd_sampled(qb, kb, vb, dob, True, scale, heads, pos, pos,
+                                       dtype="bf16")
+    sel = torch.from_numpy(pos).cuda()
+    for t, (b, h) in enumerate(heads):
+        for name, g_all, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            g = g_all[b, sel, h].double().cpu().numpy()
+            err = np.linalg.norm(g - r[t]) / np.linalg.norm(r[t])
+            mx = np.abs(g - r[t]).max() / np.abs(r[t]).max()
+            assert err <= REL_L2 and mx <= REL_MAX, (h, name, err, mx)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_masks_fp16(causal):
+    """The masked backward in fp16 (window and key lengths together)."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    B, H, N, d = 2, 3, 333, 128
+    qb, kb, vb = make_qkv(B, H, N, d, "fp16", seed=9970)
+    dob = round_to_bits(normal((B, N, H, d), 9971), "fp16")
+    q, k, v, do = (to_device(x, "fp16") for x in (qb, kb, vb, dob))
+    scale = softmax_scale(d)
+    window, lens = (90, 40), [333, 150]
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device="cuda")
+    binding.fa_fwd(q, k, v, o, lse, causal, scale, None, window, lens_t)
+    grads = [torch.full_like(q, float("nan")) for _ in range(3)]
+    binding.fa_bwd(q, k, v, o, do, lse, *grads, causal, scale, None, None, window, lens_t)
+    assert binding.device_error() == 0
+    ref = oracle.attention_bwd(qb, kb, vb, dob, causal, scale, dtype="fp16", window=window,
+                               seqlens_k=lens)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        g = g.double().cpu().numpy()
+        err = np.linalg.norm(g - r) / np.linalg.norm(r)
+        mx = np.abs(g - r).max() / np.abs(r).max()
+        assert err <= REL_L2 and mx <= REL_MAX, (name, causal, err, mx)
