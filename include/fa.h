@@ -1,5 +1,6 @@
 /*
- * fa.h -- C ABI of the fused exact attention forward for GB300 (sm_103a).
+ * fa.h -- C ABI of fused exact attention for GB300 (sm_103a): the forward (with masks and a
+ * split-K/V form), its backward, and host-buffer forms of both.
  *
  * The operation ("FlashAttention 优化原理与实现要点解析" §1, §2, §4.3, §5, §7):
  *
@@ -21,9 +22,9 @@
  * ("FlashAttention V2 核心原理与架构设计" §5.2). lse: [B, H, N] fp32, element (b, h, n) at
  * (b*H + h)*N + n.
  *
- * Ownership. Every pointer is a device pointer owned by the caller. The library allocates
- * no device memory per call and frees nothing. Calls are asynchronous: fa_fwd only enqueues
- * work on `stream` and returns.
+ * Ownership. Every pointer is owned by the caller and is a device pointer, except the host
+ * buffers of fa_fwd_host and fa_bwd_host. The library allocates no device memory per call and
+ * frees nothing. Calls are asynchronous: they only enqueue work on `stream` and return.
  *
  * Threading. The entry points are thread-safe; per-device state (the device-side error word,
  * the kernel attributes) is set up on first use of each device.
