@@ -187,3 +187,28 @@ def test_bwd_masked_host_side_checks(lib):
     # the unmasked call reaches the same checks as the masked one with no mask
     assert lib.fa_bwd(*ptrs, 2, 1, 0, 64, 0, 0.125, 0, ws, ws_bytes, None) == FA_ERR_SHAPE
     assert call(left=5, right=7) == call(left=-1, right=-1)     # only device checks remain
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/fa.h compiles as strict C99 (no CUDA headers needed: the stream is an opaque
+    pointer) and a C program calling through it links against the built library."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    from io_aware_attention_fa2_gb300 import build as fa_build
+    src = tmp_path / "use_fa.c"
+    src.write_text('#include "fa.h"\n#include <stdio.h>\n'
+                   'int main(void) {\n'
+                   '  printf("%d %s\\n", fa_abi_version(), fa_error_string(FA_ERR_SHAPE));\n'
+                   '  return fa_abi_version() == 1 ? 0 : 1;\n}\n')
+    exe = tmp_path / "use_fa"
+    lib_path = fa_build.build()
+    libdir = os.path.dirname(lib_path)
+    cmd = ["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+           "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+           "-L", libdir, "-l:" + os.path.basename(lib_path),
+           "-Wl,-rpath," + libdir]
+    subprocess.run(cmd, check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    assert out.split()[0] == "1" and "unsupported shape" in out
