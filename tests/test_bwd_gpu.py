@@ -329,3 +329,33 @@ def test_bwd_masks_fp16(causal):
         err = np.linalg.norm(g - r) / np.linalg.norm(r)
         mx = np.abs(g - r).max() / np.abs(r).max()
         assert err <= REL_L2 and mx <= REL_MAX, (name, causal, err, mx)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.09, 1.0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_scale_values(scale, causal):
+    """Scales other than 1/sqrt(d): zero (uniform P; dQ and dK vanish), negative, and 1 (large
+    logits). The forward's LSE carries the scale into P; dK and dQ take it at the end."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    B, H, N, d = 1, 3, 300, 64
+    qb, kb, vb = make_qkv(B, H, N, d, "bf16", seed=9990)
+    dob = round_to_bits(normal((B, N, H, d), 9991), "bf16")
+    q, k, v, do = (to_device(x, "bf16") for x in (qb, kb, vb, dob))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device="cuda")
+    binding.fa_fwd(q, k, v, o, lse, causal, scale)
+    grads = [torch.full_like(q, float("nan")) for _ in range(3)]
+    binding.fa_bwd(q, k, v, o, do, lse, *grads, causal, scale)
+    assert binding.device_error() == 0
+    ref = oracle.attention_bwd(qb, kb, vb, dob, causal, scale, dtype="bf16")
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        g = g.double().cpu().numpy()
+        assert np.isfinite(g).all(), name
+        if np.abs(r).max() < 1e-6:
+            assert np.abs(g).max() <= 1e-3, (name, scale, float(np.abs(g).max()))
+            continue
+        err = np.linalg.norm(g - r) / np.linalg.norm(r)
+        mx = np.abs(g - r).max() / np.abs(r).max()
+        assert err <= REL_L2 and mx <= REL_MAX, (name, scale, causal, err, mx)
