@@ -191,6 +191,19 @@ int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, fl
                 int d, int causal, float scale, int dtype, fa_stream_t stream);
 
 /*
+ * fa_fwd_host_masked -- fa_fwd_host for the attention of fa_fwd_masked: the same window
+ * (window_left, window_right) and key lengths (seqlens_k: DEVICE int32 [B], 4-byte aligned, or
+ * NULL; the head groups span every batch, so it applies to each of them unchanged). Every other
+ * argument, the streams and the return codes as in fa_fwd_host; fa_fwd_host(...) equals
+ * fa_fwd_host_masked(..., -1, -1, NULL, ...).
+ */
+int fa_fwd_host_masked(const void* q_h, const void* k_h, const void* v_h, void* o_h,
+                       float* lse_h, void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,
+                       int B, int H, int N, int d, int causal, int window_left,
+                       int window_right, const int* seqlens_k, float scale, int dtype,
+                       fa_stream_t stream);
+
+/*
  * fa_bwd -- gradients of the forward: dQ, dK, dV of L = sum(dO * O) for O = fa_fwd(q, k, v).
  * The forward keeps, per row, the softmax statistics the backward needs ("FlashAttention V2
  * 核心原理与架构设计" §2.3 keeps m and l; here their combination LSE = m + ln l), so the
@@ -256,6 +269,19 @@ int fa_bwd_host(const void* q_h, const void* k_h, const void* v_h, const void* o
                 void* dq_d, void* dk_d, void* dv_d, void* workspace, size_t workspace_bytes,
                 int B, int H, int N, int d, int causal, float scale, int dtype,
                 fa_stream_t stream);
+
+/*
+ * fa_bwd_host_masked -- fa_bwd_host for the attention of fa_bwd_masked (window and key lengths,
+ * seqlens_k a DEVICE int32 [B] array or NULL, as in fa_fwd_host_masked). Every other argument
+ * as in fa_bwd_host; fa_bwd_host(...) equals fa_bwd_host_masked(..., -1, -1, NULL, ...).
+ */
+int fa_bwd_host_masked(const void* q_h, const void* k_h, const void* v_h, const void* o_h,
+                       const void* do_h, const float* lse_h, void* dq_h, void* dk_h, void* dv_h,
+                       void* q_d, void* k_d, void* v_d, void* o_d, void* do_d, float* lse_d,
+                       void* dq_d, void* dk_d, void* dv_d, void* workspace,
+                       size_t workspace_bytes, int B, int H, int N, int d, int causal,
+                       int window_left, int window_right, const int* seqlens_k, float scale,
+                       int dtype, fa_stream_t stream);
 
 /* Static English text for a status code (never NULL). */
 const char* fa_error_string(int code);

@@ -70,6 +70,11 @@ def load_library() -> ctypes.CDLL:
             lib.fa_bwd_host.argtypes = [vp] * 19 + [ctypes.c_size_t] + [i32] * 5 + [f32, i32,
                                                                               vp]
             lib.fa_bwd_host.restype = i32
+            lib.fa_fwd_host_masked.argtypes = [vp] * 10 + [i32] * 7 + [vp, f32, i32, vp]
+            lib.fa_fwd_host_masked.restype = i32
+            lib.fa_bwd_host_masked.argtypes = ([vp] * 19 + [ctypes.c_size_t] + [i32] * 7 +
+                                               [vp, f32, i32, vp])
+            lib.fa_bwd_host_masked.restype = i32
             lib.fa_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
             lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
             lib.fa_error_string.argtypes = [i32]
@@ -304,22 +309,25 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
                                                      pin_memory=q.is_pinned())
     l_host = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32,
                                                      pin_memory=q.is_pinned())
-    plain = (not split and seqlens_k is None and tuple(window) == (-1, -1)
-             and all(t.is_contiguous() for t in (q, k, v, o_host, l_host))
+    plain = (not split and all(t.is_contiguous() for t in (q, k, v, o_host, l_host))
              and q.dtype in (torch.bfloat16, torch.float16) and k.dtype == q.dtype
              and v.dtype == q.dtype and o_host.dtype == q.dtype)
     if plain:
-        # fa_fwd_host: the library copies group of heads by group of heads, overlapping
+        # fa_fwd_host_masked: the library copies group of heads by group of heads, overlapping
         # the copies of one group with the kernel of another.
         with torch.cuda.device(dev):
             qd, kd, vd, od = (torch.empty(q.shape, dtype=q.dtype, device=dev) for _ in range(4))
             ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        rc = load_library().fa_fwd_host(
+            lens = None if seqlens_k is None else seqlens_k.to(dev, torch.int32)
+        left, right = (int(w) for w in window)
+        rc = load_library().fa_fwd_host_masked(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), o_host.data_ptr(), l_host.data_ptr(),
             qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), ld.data_ptr(),
-            B, H, N, d, int(bool(causal)), float(scale), _dtype_code(q), st.cuda_stream)
+            B, H, N, d, int(bool(causal)), left, right,
+            None if lens is None else lens.data_ptr(), float(scale), _dtype_code(q),
+            st.cuda_stream)
         if rc != 0:
-            raise FaError(rc, "fa_fwd_host")
+            raise FaError(rc, "fa_fwd_host_masked")
         st.synchronize()
         return o_host, l_host
     with torch.cuda.stream(st):
@@ -348,7 +356,6 @@ def attention_backward(q, k, v, o, dout, lse, causal: bool = False, scale: float
     B, N, H, d = q.shape
     if scale is None:
         scale = float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
-    masked = seqlens_k is not None or tuple(window) != (-1, -1)
     if q.is_cuda:
         dq, dk, dv = (torch.empty_like(q) for _ in range(3))
         lens = None if seqlens_k is None else seqlens_k.to(q.device, torch.int32)
@@ -364,30 +371,21 @@ def attention_backward(q, k, v, o, dout, lse, causal: bool = False, scale: float
     dev = torch.device(device or "cuda:0")
     st = stream if stream is not None else torch.cuda.current_stream(dev)
     host = [torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned()) for _ in range(3)]
-    if masked:
-        # masks: copies in, fa_bwd_masked, copies out, all on `st`
-        with torch.cuda.stream(st):
-            dev_in = [t.to(dev, non_blocking=True) for t in (q, k, v, o, dout, lse)]
-            grads = [torch.empty_like(dev_in[0]) for _ in range(3)]
-            lens = (None if seqlens_k is None
-                    else seqlens_k.to(dev, torch.int32, non_blocking=True))
-            fa_bwd(*dev_in, *grads, causal, scale, None, st, window, lens)
-            for h_, g_ in zip(host, grads):
-                h_.copy_(g_, non_blocking=True)
-        st.synchronize()
-        return tuple(host)
     with torch.cuda.device(dev):
         bufs = [torch.empty(q.shape, dtype=q.dtype, device=dev) for _ in range(8)]
         ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         need = bwd_workspace_size(B, H, N, d)
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
-    # fa_bwd_host: copies of one group of heads overlap the kernels of another
-    rc = load_library().fa_bwd_host(
+        lens = None if seqlens_k is None else seqlens_k.to(dev, torch.int32)
+    left, right = (int(w) for w in window)
+    # fa_bwd_host_masked: copies of one group of heads overlap the kernels of another
+    rc = load_library().fa_bwd_host_masked(
         *(t.data_ptr() for t in (q, k, v, o, dout, lse, *host)),
         *(t.data_ptr() for t in bufs[:5]), ld.data_ptr(), *(t.data_ptr() for t in bufs[5:]),
-        ws.data_ptr(), need, B, H, N, d, int(bool(causal)), float(scale), _dtype_code(q),
+        ws.data_ptr(), need, B, H, N, d, int(bool(causal)), left, right,
+        None if lens is None else lens.data_ptr(), float(scale), _dtype_code(q),
         st.cuda_stream)
     if rc != FA_OK:
-        raise FaError(rc, "fa_bwd_host")
+        raise FaError(rc, "fa_bwd_host_masked")
     st.synchronize()
     return tuple(host)

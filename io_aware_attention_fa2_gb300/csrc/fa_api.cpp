@@ -375,11 +375,13 @@ bool copy_rows(float* compact, float* host, bool to_device, int B, int N, int H,
 
 extern "C" {
 
-int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
-                void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d, int B, int H, int N,
-                int d, int causal, float scale, int dtype, fa_stream_t stream) {
+int fa_fwd_host_masked(const void* q_h, const void* k_h, const void* v_h, void* o_h,
+                       float* lse_h, void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,
+                       int B, int H, int N, int d, int causal, int window_left,
+                       int window_right, const int* seqlens_k, float scale, int dtype,
+                       fa_stream_t stream) {
   if (!q_h || !k_h || !v_h || !o_h || !lse_h) return FA_ERR_NULL;
-  int rc = check_forward(q_d, k_d, v_d, o_d, lse_d, B, H, N, N, d, dtype, scale, nullptr, 1,
+  int rc = check_forward(q_d, k_d, v_d, o_d, lse_d, B, H, N, N, d, dtype, scale, seqlens_k, 1,
                          nullptr, 0, true);
   if (rc != FA_OK) return rc;
   int device = 0, groups = 1;
@@ -415,8 +417,9 @@ int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, fl
         cudaEventRecord(ev[2 + 2 * g], hp->in) != cudaSuccess ||
         cudaStreamWaitEvent(s, ev[2 + 2 * g], 0) != cudaSuccess)
       return FA_ERR_CUDA;
-    rc = run_forward(qd, kd, vd, od, ld, B, hc, N, N, d, causal, -1, -1, nullptr, scale, dtype,
-                     1, nullptr, 0, stream);
+    // groups span every batch, so the per-batch key lengths apply to each group unchanged
+    rc = run_forward(qd, kd, vd, od, ld, B, hc, N, N, d, causal, window_left, window_right,
+                     seqlens_k, scale, dtype, 1, nullptr, 0, stream);
     if (rc != FA_OK) return rc;
     if (cudaEventRecord(ev[3 + 2 * g], s) != cudaSuccess ||
         cudaStreamWaitEvent(hp->out, ev[3 + 2 * g], 0) != cudaSuccess ||
@@ -432,16 +435,24 @@ int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, fl
   return FA_OK;
 }
 
-int fa_bwd_host(const void* q_h, const void* k_h, const void* v_h, const void* o_h,
-                const void* do_h, const float* lse_h, void* dq_h, void* dk_h, void* dv_h,
-                void* q_d, void* k_d, void* v_d, void* o_d, void* do_d, float* lse_d,
-                void* dq_d, void* dk_d, void* dv_d, void* workspace, size_t workspace_bytes,
-                int B, int H, int N, int d, int causal, float scale, int dtype,
-                fa_stream_t stream) {
+int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d, int B, int H, int N,
+                int d, int causal, float scale, int dtype, fa_stream_t stream) {
+  return fa_fwd_host_masked(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, B, H, N, d,
+                            causal, -1, -1, nullptr, scale, dtype, stream);
+}
+
+int fa_bwd_host_masked(const void* q_h, const void* k_h, const void* v_h, const void* o_h,
+                       const void* do_h, const float* lse_h, void* dq_h, void* dk_h, void* dv_h,
+                       void* q_d, void* k_d, void* v_d, void* o_d, void* do_d, float* lse_d,
+                       void* dq_d, void* dk_d, void* dv_d, void* workspace,
+                       size_t workspace_bytes, int B, int H, int N, int d, int causal,
+                       int window_left, int window_right, const int* seqlens_k, float scale,
+                       int dtype, fa_stream_t stream) {
   if (!q_h || !k_h || !v_h || !o_h || !do_h || !lse_h || !dq_h || !dk_h || !dv_h)
     return FA_ERR_NULL;
   int rc = check_backward(q_d, k_d, v_d, o_d, do_d, lse_d, dq_d, dk_d, dv_d, B, H, N, d, scale,
-                          dtype, workspace, workspace_bytes, true);
+                          dtype, workspace, workspace_bytes, true, seqlens_k);
   if (rc != FA_OK) return rc;
   int device = 0, groups = 1;
   if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
@@ -476,8 +487,9 @@ int fa_bwd_host(const void* q_h, const void* k_h, const void* v_h, const void* o
         cudaEventRecord(ev[2 + 2 * g], hp->in) != cudaSuccess ||
         cudaStreamWaitEvent(s, ev[2 + 2 * g], 0) != cudaSuccess)
       return FA_ERR_CUDA;
-    rc = fa_bwd(dev[0], dev[1], dev[2], dev[3], dev[4], ld, dev[5], dev[6], dev[7], B, hc, N, d,
-                causal, scale, dtype, workspace, workspace_bytes, stream);
+    rc = fa_bwd_masked(dev[0], dev[1], dev[2], dev[3], dev[4], ld, dev[5], dev[6], dev[7], B, hc,
+                       N, d, causal, window_left, window_right, seqlens_k, scale, dtype,
+                       workspace, workspace_bytes, stream);
     if (rc != FA_OK) return rc;
     void* outs[3] = {dq_h, dk_h, dv_h};
     if (cudaEventRecord(ev[3 + 2 * g], s) != cudaSuccess ||
@@ -492,6 +504,17 @@ int fa_bwd_host(const void* q_h, const void* k_h, const void* v_h, const void* o
   if (cudaEventRecord(ev[1], hp->out) != cudaSuccess || cudaStreamWaitEvent(s, ev[1], 0))
     return FA_ERR_CUDA;
   return FA_OK;
+}
+
+int fa_bwd_host(const void* q_h, const void* k_h, const void* v_h, const void* o_h,
+                const void* do_h, const float* lse_h, void* dq_h, void* dk_h, void* dv_h,
+                void* q_d, void* k_d, void* v_d, void* o_d, void* do_d, float* lse_d,
+                void* dq_d, void* dk_d, void* dv_d, void* workspace, size_t workspace_bytes,
+                int B, int H, int N, int d, int causal, float scale, int dtype,
+                fa_stream_t stream) {
+  return fa_bwd_host_masked(q_h, k_h, v_h, o_h, do_h, lse_h, dq_h, dk_h, dv_h, q_d, k_d, v_d,
+                            o_d, do_d, lse_d, dq_d, dk_d, dv_d, workspace, workspace_bytes, B,
+                            H, N, d, causal, -1, -1, nullptr, scale, dtype, stream);
 }
 
 int fa_selftest_wait_timeout(int limit_us, fa_stream_t stream) {

@@ -186,7 +186,6 @@ def test_bwd_masked_host_side_checks(lib):
     assert call(lens=ptrs[6] + 64) == FA_ERR_ALIAS              # key lengths inside dq
     # the unmasked call reaches the same checks as the masked one with no mask
     assert lib.fa_bwd(*ptrs, 2, 1, 0, 64, 0, 0.125, 0, ws, ws_bytes, None) == FA_ERR_SHAPE
-    assert call(left=5, right=7) == call(left=-1, right=-1)     # only device checks remain
 
 
 def test_header_is_plain_c_and_links(lib, tmp_path):
@@ -212,3 +211,27 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
     subprocess.run(cmd, check=True, capture_output=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
     assert out.split()[0] == "1" and "unsupported shape" in out
+
+
+def test_host_masked_entry_points_host_checks(lib):
+    # Fake, never dereferenced addresses: every case below fails a host-side check first.
+    h = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000]
+    dvc = [0x100000, 0x200000, 0x300000, 0x400000, 0x500000]
+
+    def fwd(lens=0, hosts=h):
+        return lib.fa_fwd_host_masked(*hosts, *dvc, 2, 1, 128, 64, 1, 32, 0, lens, 0.125, 0,
+                                      None)
+
+    assert fwd(hosts=[0] + h[1:]) == FA_ERR_NULL
+    assert fwd(lens=0x600002) == FA_ERR_ALIGN                   # key lengths not 4-byte aligned
+    assert fwd(lens=dvc[3] + 64) == FA_ERR_ALIAS                # key lengths inside o_d
+    hb = [0x1000 * (i + 1) for i in range(9)]
+    db = [0x100000 * (i + 1) for i in range(9)]
+    ws, ws_bytes = 0x100000 * 10, int(lib.fa_bwd_workspace_size(2, 1, 128, 64))
+
+    def bwd(lens=0):
+        return lib.fa_bwd_host_masked(*hb, *db, ws, ws_bytes, 2, 1, 128, 64, 0, 16, 16, lens,
+                                      0.125, 0, None)
+
+    assert bwd(lens=0xB00002) == FA_ERR_ALIGN
+    assert bwd(lens=db[7] + 64) == FA_ERR_ALIAS                 # key lengths inside dk_d

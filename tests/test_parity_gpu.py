@@ -202,3 +202,32 @@ def test_long_sequence_d64_sampled():
     rb, rh, ri = (torch.from_numpy(rows[:, c]).cuda() for c in range(3))
     assert_close(o[rb, ri, rh].double().cpu().numpy(), lse[rb, rh, ri].double().cpu().numpy(),
                  o_ref, lse_ref, "N=32768 d=64")
+
+
+@pytest.mark.parametrize("window,lens,causal", [((100, 0), None, True),
+                                                ((-1, -1), [1000, 333], False),
+                                                ((64, 64), None, False),
+                                                ((300, -1), [1000, 900], True)])
+def test_masked_host_entry_matches_device_path(window, lens, causal):
+    """fa_fwd_host_masked (host buffers with the window and key-length masks) gives exactly the
+    device path's O and LSE."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    B, H, N, d = 2, 6, 1000, 128
+    qb, kb, vb = make_qkv(B, H, N, d, "bf16", seed=8700 + (lens[1] if lens else 0))
+    hq, hk, hv = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for x in (qb, kb, vb))
+    lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32)
+    o_h, l_h = binding.attention_forward(hq, hk, hv, causal=causal, window=window,
+                                         seqlens_k=lens_t)
+    o_d, l_d = binding.attention_forward(hq.cuda(), hk.cuda(), hv.cuda(), causal=causal,
+                                         window=window,
+                                         seqlens_k=None if lens_t is None else lens_t.cuda())
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    assert torch.equal(o_h.view(torch.int16), o_d.cpu().view(torch.int16))
+    assert torch.equal(l_h, l_d.cpu())
+    o_ref, lse_ref = oracle.attention(qb, kb, vb, causal, softmax_scale(d), dtype="bf16",
+                                      window=window, seqlens_k=lens)
+    assert_close(o_h.double().numpy(), l_h.double().numpy(), o_ref, lse_ref, "host masked")
