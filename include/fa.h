@@ -60,7 +60,8 @@ enum fa_status {
     FA_ERR_TIMEOUT = -8,  /* a kernel wait ran past its limit; outputs are undefined */
     FA_ERR_SCALE = -9,    /* scale is not finite */
     FA_ERR_CUDA = -10,    /* a CUDA runtime or driver query failed */
-    FA_ERR_WORKSPACE = -11  /* workspace smaller than fa_fwd_splitkv_workspace_size() */
+    FA_ERR_WORKSPACE = -11, /* workspace smaller than fa_fwd_splitkv_workspace_size() */
+    FA_ERR_POINTER = -12    /* a device-side argument is not device memory of the current device */
 };
 
 /*
@@ -78,9 +79,11 @@ enum fa_status {
  *   stream   CUDA stream the work is enqueued on
  *
  * Returns FA_OK once the work is enqueued. On a host-detected error (every code except
- * FA_ERR_TIMEOUT) nothing is enqueued and the outputs are untouched. Kernel waits are bounded:
- * if one runs out, the kernel records FA_ERR_TIMEOUT in a per-device error word (read it with
- * fa_get_device_error) and exits without hanging the device.
+ * FA_ERR_TIMEOUT) nothing is enqueued and the outputs are untouched. Every device-side pointer
+ * is looked up (cudaPointerGetAttributes) before anything is enqueued: host memory, memory of
+ * another device or an unknown address gives FA_ERR_POINTER instead of a faulting kernel.
+ * Kernel waits are bounded: if one runs out, the kernel records FA_ERR_TIMEOUT in a per-device
+ * error word (read it with fa_get_device_error) and exits without hanging the device.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
            int N, int d, int causal, float scale, int dtype, fa_stream_t stream);

@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <initializer_list>
 #include <mutex>
 #include <vector>
 
@@ -55,6 +56,22 @@ int check_arch(int* device) {
   return state == 1 ? FA_OK : FA_ERR_ARCH;
 }
 
+// Every non-null pointer must be device (or managed) memory usable by `device`: a host or
+// unknown address would make the kernels fault, so it is refused before anything is enqueued.
+int check_device_ptrs(int device, std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs) {
+    if (!p) continue;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      cudaGetLastError();   // not sticky; leave no error behind for the caller
+      return FA_ERR_POINTER;
+    }
+    if (a.type == cudaMemoryTypeManaged) continue;
+    if (a.type != cudaMemoryTypeDevice || a.device != device) return FA_ERR_POINTER;
+  }
+  return FA_OK;
+}
+
 bool overlaps(const void* a, uint64_t a_bytes, const void* b, uint64_t b_bytes) {
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
   return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
@@ -99,6 +116,8 @@ const char* fa_error_string(int code) {
     case FA_ERR_SCALE: return "scale is not finite";
     case FA_ERR_CUDA: return "a CUDA runtime or driver call failed";
     case FA_ERR_WORKSPACE: return "workspace smaller than fa_fwd_splitkv_workspace_size()";
+    case FA_ERR_POINTER:
+      return "a device-side argument is not device memory of the current device";
     default: return "unknown status";
   }
 }
@@ -157,7 +176,10 @@ int check_forward(const void* q, const void* k, const void* v, void* o, float* l
       for (int j = i + 1; j < 3; ++j)
         if (overlaps(ins[i].p, ins[i].n, ins[j].p, ins[j].n)) return FA_ERR_ALIAS;
   int device = 0;
-  return check_arch(&device);
+  const int rc = check_arch(&device);
+  if (rc != FA_OK) return rc;
+  return check_device_ptrs(device, {q, k, v, o, lse, seqlens_k,
+                                    num_splits > 1 ? workspace : nullptr});
 }
 
 // Shared checks and launch of every forward entry point.
@@ -291,7 +313,9 @@ int check_backward(const void* q, const void* k, const void* v, const void* o,
       for (int j = i + 1; j < 6; ++j)
         if (overlaps(ins[i].p, ins[i].n, ins[j].p, ins[j].n)) return FA_ERR_ALIAS;
   int device = 0;
-  return check_arch(&device);
+  const int rc = check_arch(&device);
+  if (rc != FA_OK) return rc;
+  return check_device_ptrs(device, {q, k, v, o, dout, lse, dq, dk, dv, workspace, seqlens_k});
 }
 
 }  // namespace

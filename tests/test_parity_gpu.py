@@ -231,3 +231,31 @@ def test_masked_host_entry_matches_device_path(window, lens, causal):
     o_ref, lse_ref = oracle.attention(qb, kb, vb, causal, softmax_scale(d), dtype="bf16",
                                       window=window, seqlens_k=lens)
     assert_close(o_h.double().numpy(), l_h.double().numpy(), o_ref, lse_ref, "host masked")
+
+
+def test_non_device_pointers_are_refused_before_launch():
+    """Host memory passed where device memory is expected returns FA_ERR_POINTER and launches
+    nothing; device memory of the current device passes. The case checked puts the LSE output
+    in pinned host memory, which a kernel could even write safely (mapped host memory), so the
+    test runs nothing that could fault should the check ever let it through."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    lib = binding.load_library()
+    B, H, N, d = 1, 2, 256, 64
+    q = torch.randn(B, N, H, d, device="cuda").to(torch.bfloat16)
+    k, v, o = torch.randn_like(q), torch.randn_like(q), torch.zeros_like(q)
+    lse = torch.zeros(B, H, N, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    bad_lse = torch.zeros(B, H, N).pin_memory()
+    assert lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), bad_lse.data_ptr(),
+                      B, H, N, d, 0, 0.125, 0, st) == -12
+    torch.cuda.synchronize()
+    assert int(o.view(torch.int16).abs().sum()) == 0          # nothing ran
+    assert float(bad_lse.abs().sum()) == 0.0
+    assert lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B,
+                      H, N, d, 0, 0.125, 0, st) == 0
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    assert lib.fa_error_string(-12) == (
+        b"a device-side argument is not device memory of the current device")
