@@ -184,9 +184,10 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
  *   B, H, N, d, causal, scale, dtype: as in fa_fwd
  * Page-locked (pinned) host memory lets the copies run asynchronously; with pageable memory
  * the call is still correct but the copies do not overlap. Work is enqueued on `stream` and on
- * two copy streams the library keeps per device; `stream` reaches completion (O and LSE in host
- * memory) after everything enqueued here, so synchronise `stream` before reading o_h, lse_h,
- * and keep every buffer alive until then. Returns as fa_fwd; on a host-detected error nothing is
+ * two copy streams and three kernel streams the library keeps per device (the groups' kernels
+ * take the kernel streams in turn, so that they overlap one another); `stream` reaches
+ * completion (O and LSE in host memory) after everything enqueued here, so synchronise
+ * `stream` before reading o_h, lse_h, and keep every buffer alive until then. Returns as fa_fwd; on a host-detected error nothing is
  * enqueued. Calls from several threads are serialised while they enqueue.
  */
 int fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
@@ -261,7 +262,11 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   dq_h, dk_h, dv_h  [B, N, H, d] dtype, host memory: outputs
  *   q_d ... dv_d   device buffers of the same sizes, owned by the caller, pairwise disjoint,
  *                  16-byte aligned (lse_d 4-byte); their previous contents are overwritten
- *   workspace      as in fa_bwd for the whole problem (every group reuses it in turn)
+ *   workspace      as in fa_bwd for the whole problem. With at least
+ *                  fa_bwd_workspace_size(B, H, N, d) + 128 bytes every group gets a part of its
+ *                  own (at a 16-byte aligned offset) and the groups' kernels overlap on the
+ *                  kernel streams; with less, the groups run one after another and reuse the
+ *                  start of it in turn
  *   B, H, N, d, causal, scale, dtype: as in fa_bwd
  * Streams, pinned memory, synchronisation and errors as in fa_fwd_host: synchronise `stream`
  * before reading dq_h, dk_h, dv_h.

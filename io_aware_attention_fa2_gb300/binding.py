@@ -374,7 +374,9 @@ def attention_backward(q, k, v, o, dout, lse, causal: bool = False, scale: float
     with torch.cuda.device(dev):
         bufs = [torch.empty(q.shape, dtype=q.dtype, device=dev) for _ in range(8)]
         ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        need = bwd_workspace_size(B, H, N, d)
+        # 128 bytes beyond the whole problem's size: every head group gets a part of its own,
+        # so that the groups' kernels overlap
+        need = bwd_workspace_size(B, H, N, d) + 128
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
         lens = None if seqlens_k is None else seqlens_k.to(dev, torch.int32)
     left, right = (int(w) for w in window)

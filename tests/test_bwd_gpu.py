@@ -151,6 +151,47 @@ def test_bwd_host_entry_matches_device_path(B, H, N, d, causal, pinned):
     assert (dq_h - dq_d).abs().le(2.0 ** -7 * dq_d.abs() + 1e-6).all()
 
 
+def test_bwd_host_workspace_with_and_without_headroom():
+    """fa_bwd_host with exactly fa_bwd_workspace_size bytes (3 head groups whose own parts would
+    need padding to 16 bytes, so they run one after another in the start of it) and with 128
+    bytes more (each group in a part of its own, the groups' kernels overlapping): both give the
+    device path's gradients."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    B, H, N, d, causal = 1, 6, 4097, 128, True
+    assert (B * (H // 3) * N) % 4 != 0   # a group's part is not a multiple of 16 bytes
+    qb, kb, vb = make_qkv(B, H, N, d, "bf16", seed=8700)
+    dob = round_to_bits(normal((B, N, H, d), 8701), "bf16")
+    host = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+            for x in (qb, kb, vb, dob)]
+    dev = [t.cuda() for t in host]
+    o, lse = binding.attention_forward(*dev[:3], causal=causal)
+    g_d = [t.cpu() for t in binding.attention_backward(*dev[:3], o, dev[3], lse, causal=causal)]
+    o_h, lse_h = o.cpu().pin_memory(), lse.cpu().pin_memory()
+    lib = binding.load_library()
+    scale = softmax_scale(d)
+    need = binding.bwd_workspace_size(B, H, N, d)
+    for extra in (0, 128):
+        outs = [torch.full_like(host[0], float("nan")).pin_memory() for _ in range(3)]
+        bufs = [torch.empty_like(dev[0]) for _ in range(8)]
+        ld = torch.empty(B, H, N, device="cuda")
+        ws = torch.empty(need + extra, dtype=torch.uint8, device="cuda")
+        st = torch.cuda.current_stream()
+        rc = lib.fa_bwd_host(*(t.data_ptr() for t in (*host[:3], o_h, host[3], lse_h, *outs)),
+                             *(t.data_ptr() for t in bufs[:5]), ld.data_ptr(),
+                             *(t.data_ptr() for t in bufs[5:]), ws.data_ptr(), need + extra,
+                             B, H, N, d, int(causal), scale, 0, st.cuda_stream)
+        assert rc == 0, binding.error_string(rc)
+        st.synchronize()
+        assert binding.device_error() == 0
+        for name, a, b in zip(("dk", "dv"), outs[1:], g_d[1:]):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (extra, name)
+        dq_h, dq_d = outs[0].double(), g_d[0].double()
+        assert torch.isfinite(dq_h).all(), extra
+        assert (dq_h - dq_d).abs().le(2.0 ** -7 * dq_d.abs() + 1e-6).all(), extra
+
+
 def run_masked_case(B, H, N, d, causal, window, lens, seed):
     """fa_fwd / fa_bwd with the window and key-length masks against the oracle's gradients of
     the same masked attention."""
