@@ -157,12 +157,20 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Waits until the kernels this grid depends on (launched before it on the stream with
+// programmatic stream serialisation) have completed and their writes are visible; returns at
+// once when there is no such dependency.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // dQ[b, q, h, :] (input type) = scale x the workspace row [b, h, q, :] (which holds
 // sum_j dS_qj k_j). One warp per (b, q, h) row, 4 elements per lane.
 template <int D, bool FP16>
 __global__ void __launch_bounds__(256)
     fa_bwd_post_kernel(const float* __restrict__ dq_acc, void* __restrict__ dq, float scale,
                        int H, int N, long long rows) {
+  grid_dependency_wait();   // the main kernel's dQ partial sums
   const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
   if (row >= rows) return;
   const int lane = threadIdx.x % 32;
@@ -324,6 +332,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto wait_w = [&](int slot, uint32_t parity) {
     return ptx::wait_bounded(bar(slot), parity, abort_p, kWaitLimitNs);
   };
+  // D and the cleared dQ workspace come from the pre kernel, which may still be finishing:
+  // the warps that read or reduce into them wait for it (the loads of K, V, Q, dO go ahead).
+  if (warp >= 2) grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -672,14 +683,29 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   const long long bytes_per_head = 8ll * p.N * p.d;
   const int heads_per_group =
       static_cast<int>(std::max(1ll, std::min(bh, (64ll << 20) / bytes_per_head)));
-  kernel<<<static_cast<unsigned>(num_kv * bh), kBwdThreads, smem, stream>>>(
-      p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.lse, p.dpre, p.dq_acc, p.dk, p.dv, p.H, p.N, p.causal,
-      p.window_left, p.window_right, p.seqlens_k, p.scale, p.scale * kLog2e, heads_per_group);
-  err = cudaGetLastError();
+  // The main and post kernels are launched with programmatic stream serialisation: each may
+  // start (set-up, independent loads) while the kernel before it finishes, and waits for it
+  // in the kernel before touching what it wrote.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_kv * bh));
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kernel, p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.lse,
+                           static_cast<const float*>(p.dpre), p.dq_acc, p.dk, p.dv, p.H, p.N,
+                           p.causal, p.window_left, p.window_right, p.seqlens_k, p.scale,
+                           p.scale * kLog2e, heads_per_group);
   if (err != cudaSuccess) return err;
-  fa_bwd_post_kernel<D, FP16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      p.dq_acc, p.dq, p.scale, p.H, p.N, rows);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, fa_bwd_post_kernel<D, FP16>,
+                            static_cast<const float*>(p.dq_acc), p.dq, p.scale, p.H, p.N, rows);
 }
 
 }  // namespace
