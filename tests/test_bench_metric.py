@@ -69,3 +69,15 @@ def test_reference_arm_reports_the_gpu_arms_metric():
     assert bench.metric_name(WORKLOADS[bench.DEFAULT_WORKLOAD], False) in names
     assert len(names) == 2
     assert "bwd" in bench.metric_name(WORKLOADS[bench.DEFAULT_WORKLOAD], True)
+
+
+def test_algorithmic_bytes_and_warm_l2_selection():
+    """Q, K, V read and O written at 2 bytes an element plus the fp32 LSE, counted by hand for
+    the headline shape; only the workloads whose data fits well inside L2 (the N = 256 and
+    N = 1K ones) get the supplementary timing without the L2 flush."""
+    w = WORKLOADS["n8k_d128_causal"]
+    assert bench.algorithmic_bytes(w) == 4 * 2 * 8192 * 16 * 128 * 2 + 2 * 16 * 8192 * 4
+    small = {n for n, x in WORKLOADS.items()
+             if bench.algorithmic_bytes(x) < bench.WARM_L2_MAX_BYTES}
+    assert small == {"tiny_n256_d64", "n1k_d64", "n1k_d64_causal", "n1k_d128"}
+    assert bench.WARM_L2_MAX_BYTES < bench.L2_FLUSH_BYTES
