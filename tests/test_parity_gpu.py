@@ -145,9 +145,9 @@ def test_user_api_host_and_device_tensors():
 
 @pytest.mark.parametrize("B,H,N,d,causal,pinned", [
     (1, 4, 200, 64, True, True), (3, 4, 1000, 128, False, True), (5, 4, 333, 128, True, False),
-    (2, 16, 8192, 128, True, True),     # 3 head groups of 5, 5, 6 heads
-    (3, 11, 8192, 64, False, True),     # 3 uneven groups
-    (1, 12, 16384, 128, True, False)])  # 2 groups, pageable host memory
+    (2, 16, 8192, 128, True, True),     # 8 head groups of 2 heads
+    (3, 11, 8192, 64, False, True),     # 8 unequal groups (11 has no divisor from 4 to 8)
+    (1, 12, 16384, 128, True, False)])  # 6 groups of 2 heads, pageable host memory
 def test_host_entry_matches_device_path(B, H, N, d, causal, pinned):
     """fa_fwd_host (host buffers, head groups packed by pitched copies, copies overlapping the
     kernels) gives exactly the device path's O and LSE: the same kernel on the same values."""
