@@ -36,7 +36,9 @@
  * key lengths are int32 [B].
  *
  * There is no blocking, fusion or reordering here: one (b, h, i) row at a time, the three
- * passes in order. Rows are independent, so OpenMP spreads rows over host cores.
+ * passes in order. Rows are independent, so OpenMP spreads rows over host cores. The bf16 /
+ * fp16 inputs are decoded to their exact fp64 values once per call, before any arithmetic
+ * (decoding is exact, so this changes no result, only the cost of re-reading an element).
  */
 #include <math.h>
 #include <stdint.h>
@@ -86,6 +88,48 @@ int oracle_decode(const uint16_t* bits, int64_t n, int kind, double* out) {
     return 0;
 }
 
+/* The exact fp64 values of n input elements of the given kind. fp64 inputs are used in place
+ * (*owned = 0); bf16 / fp16 ones are decoded into a new array (*owned = 1, free it). Returns
+ * NULL when memory runs out. */
+static const double* as_f64(const void* base, int kind, int64_t n, int* owned) {
+    *owned = 0;
+    if (kind == ORACLE_F64) return (const double*)base;
+    double* out = (double*)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    if (!out) return NULL;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) out[t] = elem(base, kind, t);
+    *owned = 1;
+    return out;
+}
+
+/* The decoded inputs of one call. */
+typedef struct {
+    const double *q, *k, *v, *g;   /* g: the upstream gradient (backward only) */
+    int own_q, own_k, own_v, own_g;
+} Decoded;
+
+static void release(Decoded* x) {
+    if (x->own_q) free((void*)x->q);
+    if (x->own_k) free((void*)x->k);
+    if (x->own_v) free((void*)x->v);
+    if (x->own_g) free((void*)x->g);
+}
+
+/* Decode q (nq elements), k, v (nk each) and optionally dout (nq). Returns 0 or -4. */
+static int decode_inputs(const void* q, const void* k, const void* v, const void* dout, int kind,
+                         int64_t nq, int64_t nk, Decoded* x) {
+    memset(x, 0, sizeof *x);
+    x->q = as_f64(q, kind, nq, &x->own_q);
+    x->k = as_f64(k, kind, nk, &x->own_k);
+    x->v = as_f64(v, kind, nk, &x->own_v);
+    if (dout) x->g = as_f64(dout, kind, nq, &x->own_g);
+    if (!x->q || !x->k || !x->v || (dout && !x->g)) {
+        release(x);
+        return -4;
+    }
+    return 0;
+}
+
 /* The keys query i may attend to: [lo, hi). `len_b` is the batch's key length; `pos` is the
  * query's position in the key sequence (i + Nk - Nq). */
 static void key_range(int64_t pos, int causal, int64_t wl, int64_t wr, int64_t len_b,
@@ -99,7 +143,7 @@ static void key_range(int64_t pos, int causal, int64_t wl, int64_t wr, int64_t l
 }
 
 /* One output row: query i of head (b, h) over keys [lo, hi). `s` is scratch of >= Nk doubles. */
-static void attention_row(const void* q, const void* k, const void* v, int kind,
+static void attention_row(const double* q, const double* k, const double* v,
                           int64_t Nq, int64_t Nk, int64_t H, int64_t d, int64_t lo, int64_t hi,
                           double scale, int64_t b, int64_t h, int64_t i, double* s,
                           double* o_row, double* lse_out) {
@@ -114,7 +158,7 @@ static void attention_row(const void* q, const void* k, const void* v, int kind,
     for (int64_t j = lo; j < hi; ++j) {
         const int64_t k_off = ((b * Nk + j) * H + h) * d;
         double dot = 0.0;
-        for (int64_t c = 0; c < d; ++c) dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);
+        for (int64_t c = 0; c < d; ++c) dot += q[q_off + c] * k[k_off + c];
         s[j] = scale * dot;
     }
 
@@ -134,7 +178,7 @@ static void attention_row(const void* q, const void* k, const void* v, int kind,
     for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
     for (int64_t j = lo; j < hi; ++j) {
         const int64_t v_off = ((b * Nk + j) * H + h) * d;
-        for (int64_t c = 0; c < d; ++c) o_row[c] += s[j] * elem(v, kind, v_off + c);
+        for (int64_t c = 0; c < d; ++c) o_row[c] += s[j] * v[v_off + c];
     }
 
     *lse_out = m + log(l);
@@ -163,6 +207,8 @@ int oracle_attention_qk(const void* q, const void* k, const void* v, int kind, i
     int rc = check_args(q, k, v, kind, B, H, Nq, Nk, d);
     if (rc) return rc;
     if (!o || !lse) return -1;
+    Decoded x;
+    if (decode_inputs(q, k, v, NULL, kind, B * Nq * H * d, B * Nk * H * d, &x)) return -4;
     const int64_t rows = B * H * Nq;
     int failed = 0;
 #pragma omp parallel
@@ -179,12 +225,13 @@ int oracle_attention_qk(const void* q, const void* k, const void* v, int kind, i
                 int64_t lo, hi;
                 key_range(i + Nk - Nq, causal, window_left, window_right,
                           batch_key_length(seqlens_k, b, Nk), &lo, &hi);
-                attention_row(q, k, v, kind, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,
+                attention_row(x.q, x.k, x.v, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,
                               o + ((b * Nq + i) * H + h) * d, lse + (b * H + h) * Nq + i);
             }
             free(s);
         }
     }
+    release(&x);
     return failed ? -4 : 0;
 }
 
@@ -215,6 +262,8 @@ int oracle_attention_rows_qk(const void* q, const void* k, const void* v, int ki
         const int64_t b = rows[3 * t], h = rows[3 * t + 1], i = rows[3 * t + 2];
         if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= Nq) return -5;
     }
+    Decoded x;
+    if (decode_inputs(q, k, v, NULL, kind, B * Nq * H * d, B * Nk * H * d, &x)) return -4;
     int failed = 0;
 #pragma omp parallel
     {
@@ -229,12 +278,13 @@ int oracle_attention_rows_qk(const void* q, const void* k, const void* v, int ki
                 int64_t lo, hi;
                 key_range(i + Nk - Nq, causal, window_left, window_right,
                           batch_key_length(seqlens_k, b, Nk), &lo, &hi);
-                attention_row(q, k, v, kind, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,
+                attention_row(x.q, x.k, x.v, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,
                               o_rows + t * d, lse_rows + t);
             }
             free(s);
         }
     }
+    release(&x);
     return failed ? -4 : 0;
 }
 
@@ -285,6 +335,9 @@ int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, co
             heads[2 * t + 1] >= H) return -2;
     for (int64_t t = 0; t < nkeys; ++t) if (keys[t] < 0 || keys[t] >= N) return -2;
     for (int64_t t = 0; t < nqueries; ++t) if (queries[t] < 0 || queries[t] >= N) return -2;
+    Decoded x;
+    if (decode_inputs(q, k, v, dout, kind, B * N * H * d, B * N * H * d, &x)) return -4;
+    const double *qd = x.q, *kd = x.k, *vd = x.v, *gd = x.g;
     double* m = (double*)malloc((size_t)N * sizeof(double));
     double* l = (double*)malloc((size_t)N * sizeof(double));
     double* D = (double*)malloc((size_t)N * sizeof(double));
@@ -292,6 +345,7 @@ int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, co
         free(m);
         free(l);
         free(D);
+        release(&x);
         return -4;
     }
     for (int64_t t = 0; t < nheads; ++t) {
@@ -307,15 +361,15 @@ int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, co
             for (int64_t j = lo; j < hi; ++j) {
                 double dot = 0.0;
                 for (int64_t c = 0; c < d; ++c)
-                    dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
+                    dot += qd[ROW(i) + c] * kd[ROW(j) + c];
                 if (scale * dot > mi) mi = scale * dot;
             }
             double li = 0.0, di = 0.0;
             for (int64_t j = lo; j < hi; ++j) {
                 double dot = 0.0, dp = 0.0;
                 for (int64_t c = 0; c < d; ++c) {
-                    dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
-                    dp += elem(dout, kind, ROW(i) + c) * elem(v, kind, ROW(j) + c);
+                    dot += qd[ROW(i) + c] * kd[ROW(j) + c];
+                    dp += gd[ROW(i) + c] * vd[ROW(j) + c];
                 }
                 const double e = exp(scale * dot - mi);
                 li += e;
@@ -338,14 +392,14 @@ int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, co
                 if (j < lo || j >= hi) continue;
                 double dot = 0.0, dp = 0.0;
                 for (int64_t c = 0; c < d; ++c) {
-                    dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
-                    dp += elem(dout, kind, ROW(i) + c) * elem(v, kind, ROW(j) + c);
+                    dot += qd[ROW(i) + c] * kd[ROW(j) + c];
+                    dp += gd[ROW(i) + c] * vd[ROW(j) + c];
                 }
                 const double p = exp(scale * dot - m[i]) / l[i];
                 const double ds = p * (dp - D[i]);
                 for (int64_t c = 0; c < d; ++c) {
-                    gv[c] += p * elem(dout, kind, ROW(i) + c);
-                    gk[c] += ds * elem(q, kind, ROW(i) + c);
+                    gv[c] += p * gd[ROW(i) + c];
+                    gk[c] += ds * qd[ROW(i) + c];
                 }
             }
             for (int64_t c = 0; c < d; ++c) gk[c] *= scale;
@@ -361,11 +415,11 @@ int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, co
             for (int64_t j = lo; j < hi; ++j) {
                 double dot = 0.0, dp = 0.0;
                 for (int64_t c = 0; c < d; ++c) {
-                    dot += elem(q, kind, ROW(i) + c) * elem(k, kind, ROW(j) + c);
-                    dp += elem(dout, kind, ROW(i) + c) * elem(v, kind, ROW(j) + c);
+                    dot += qd[ROW(i) + c] * kd[ROW(j) + c];
+                    dp += gd[ROW(i) + c] * vd[ROW(j) + c];
                 }
                 const double ds = exp(scale * dot - m[i]) / l[i] * (dp - D[i]);
-                for (int64_t c = 0; c < d; ++c) gq[c] += ds * elem(k, kind, ROW(j) + c);
+                for (int64_t c = 0; c < d; ++c) gq[c] += ds * kd[ROW(j) + c];
             }
             for (int64_t c = 0; c < d; ++c) gq[c] *= scale;
         }
@@ -374,6 +428,7 @@ int oracle_attention_bwd_sampled(const void* q, const void* k, const void* v, co
     free(m);
     free(l);
     free(D);
+    release(&x);
     return 0;
 }
 
@@ -402,6 +457,9 @@ int oracle_attention_bwd(const void* q, const void* k, const void* v, const void
     int rc = check_args(q, k, v, kind, B, H, N, N, d);
     if (rc) return rc;
     if (!dout || !dq || !dk || !dv) return -1;
+    Decoded x;
+    if (decode_inputs(q, k, v, dout, kind, B * N * H * d, B * N * H * d, &x)) return -4;
+    const double *qd = x.q, *kd = x.k, *vd = x.v, *gd = x.g;
     int failed = 0;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t bh = 0; bh < B * H; ++bh) {
@@ -427,7 +485,7 @@ int oracle_attention_bwd(const void* q, const void* k, const void* v, const void
                 const int64_t k_off = ((b * N + j) * H + h) * d;
                 double dot = 0.0;
                 for (int64_t c = 0; c < d; ++c)
-                    dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);
+                    dot += qd[q_off + c] * kd[k_off + c];
                 P[i * N + j] = scale * dot;
                 if (P[i * N + j] > m) m = P[i * N + j];
             }
@@ -444,7 +502,7 @@ int oracle_attention_bwd(const void* q, const void* k, const void* v, const void
                 const int64_t v_off = ((b * N + j) * H + h) * d;
                 double dp = 0.0;
                 for (int64_t c = 0; c < d; ++c)
-                    dp += elem(dout, kind, o_off + c) * elem(v, kind, v_off + c);
+                    dp += gd[o_off + c] * vd[v_off + c];
                 dS[i * N + j] = dp;
                 Di += P[i * N + j] * dp;
             }
@@ -457,7 +515,7 @@ int oracle_attention_bwd(const void* q, const void* k, const void* v, const void
             for (int64_t j = 0; j < N; ++j) {
                 if (dS[i * N + j] == 0.0) continue;
                 const int64_t k_off = ((b * N + j) * H + h) * d;
-                for (int64_t c = 0; c < d; ++c) out[c] += dS[i * N + j] * elem(k, kind, k_off + c);
+                for (int64_t c = 0; c < d; ++c) out[c] += dS[i * N + j] * kd[k_off + c];
             }
             for (int64_t c = 0; c < d; ++c) out[c] *= scale;
         }
@@ -470,14 +528,15 @@ int oracle_attention_bwd(const void* q, const void* k, const void* v, const void
                 const int64_t row = ((b * N + i) * H + h) * d;
                 const double ds = dS[i * N + j], p = P[i * N + j];
                 if (ds != 0.0)
-                    for (int64_t c = 0; c < d; ++c) gk[c] += ds * elem(q, kind, row + c);
+                    for (int64_t c = 0; c < d; ++c) gk[c] += ds * qd[row + c];
                 if (p != 0.0)
-                    for (int64_t c = 0; c < d; ++c) gv[c] += p * elem(dout, kind, row + c);
+                    for (int64_t c = 0; c < d; ++c) gv[c] += p * gd[row + c];
             }
             for (int64_t c = 0; c < d; ++c) gk[c] *= scale;
         }
         free(P);
         free(dS);
     }
+    release(&x);
     return failed ? -4 : 0;
 }

@@ -13,8 +13,8 @@ MUTANTS = [
     ("normalise_without_shift", "s[j] = exp(s[j] - m) / l;", "s[j] = exp(s[j]) / l;"),
     ("wrong_sign_in_exp", "s[j] = exp(s[j] - m) / l;", "s[j] = exp(m - s[j]) / l;"),
     ("transposed_q_k",
-     "for (int64_t c = 0; c < d; ++c) dot += elem(q, kind, q_off + c) * elem(k, kind, k_off + c);",
-     "for (int64_t c = 0; c < d; ++c) dot += elem(k, kind, q_off + c) * elem(q, kind, k_off + c);"),
+     "for (int64_t c = 0; c < d; ++c) dot += q[q_off + c] * k[k_off + c];",
+     "for (int64_t c = 0; c < d; ++c) dot += k[q_off + c] * q[k_off + c];"),
     ("query_row_for_value", "const int64_t v_off = ((b * Nk + j) * H + h) * d;",
      "const int64_t v_off = ((b * Nk + i) * H + h) * d;"),
     ("causal_excludes_diagonal", "if (causal && pos + 1 < z) z = pos + 1;",
@@ -27,11 +27,11 @@ MUTANTS = [
     ("query_position_not_offset",
      "key_range(i + Nk - Nq, causal, window_left, window_right,\n"
      "                          batch_key_length(seqlens_k, b, Nk), &lo, &hi);\n"
-     "                attention_row(q, k, v, kind, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,\n"
+     "                attention_row(x.q, x.k, x.v, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,\n"
      "                              o + ((b",
      "key_range(i, causal, window_left, window_right,\n"
      "                          batch_key_length(seqlens_k, b, Nk), &lo, &hi);\n"
-     "                attention_row(q, k, v, kind, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,\n"
+     "                attention_row(x.q, x.k, x.v, Nq, Nk, H, d, lo, hi, scale, b, h, i, s,\n"
      "                              o + ((b"),
     ("padding_ignored", "if (!seqlens_k) return N;", "return N;"),
     ("empty_row_lse_zero", "*lse_out = -INFINITY;", "*lse_out = 0.0;"),
