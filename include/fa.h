@@ -156,12 +156,17 @@ int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int num_sms);
  *   - Calls whose parts need more than 8 MiB (fa_fwd_splitkv_workspace_size(B, H, Nq, d,
  *     num_splits) > 8 MiB) return FA_ERR_WORKSPACE and enqueue nothing; use fewer parts, or
  *     fa_fwd_splitkv with a workspace of your own.
- *   - The first call on each device looks up the buffer's device address (once, with that
- *     device current); make that first call before any stream capture.
+ *   - The first call on each device looks up the buffer's device address (with that device
+ *     current) and keeps it for the device's context; after a device reset the next call looks
+ *     it up again. Make the first call on a device, and the first after a reset, before any
+ *     stream capture.
  *   - All calls on a device share the buffer, which keeps the last call's contents. Nothing in
  *     it needs clearing: each call writes every part it reads. Calls that overlap on the GPU
  *     (on different streams without ordering between them) race on the buffer.
- *   - Every argument means what it means for fa_fwd_splitkv; the return codes are the same.
+ *   - Every argument means what it means for fa_fwd_splitkv, and is checked in the same way
+ *     first, with the same return codes; only then are parts that do not fit the buffer
+ *     refused (FA_ERR_WORKSPACE). A failed address lookup returns FA_ERR_CUDA and leaves no
+ *     CUDA error pending.
  */
 int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int H, int Nq, int Nk, int d, int causal, int window_left,

@@ -127,10 +127,12 @@ const char* fa_error_string(int code) {
 namespace {
 
 // Host-side checks shared by every forward entry point (nothing is enqueued).
+// check_workspace = false skips the checks of the workspace argument (the caller supplies a
+// workspace of its own afterwards).
 int check_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                   int H, int Nq, int Nk, int d, int dtype, float scale, const int* seqlens_k,
                   int num_splits, void* workspace, size_t workspace_bytes,
-                  bool inputs_written = false) {
+                  bool inputs_written = false, bool check_workspace = true) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (B < 1 || H < 1 || Nq < 1 || Nk < Nq || (d != 64 && d != 128)) return FA_ERR_SHAPE;
   if (num_splits < 1 || num_splits > fa::MAX_SPLITS) return FA_ERR_SHAPE;
@@ -147,7 +149,8 @@ int check_forward(const void* q, const void* k, const void* v, void* o, float* l
   const uint64_t q_bytes = bh * (uint64_t)Nq * d * 2, k_bytes = k_elems * 2;
   const uint64_t lse_bytes = bh * (uint64_t)Nq * 4;
   const uint64_t ws_need = fa_fwd_splitkv_workspace_size(B, H, Nq, d, num_splits);
-  if (num_splits > 1) {
+  if (!check_workspace) workspace = nullptr;
+  if (num_splits > 1 && check_workspace) {
     if (!workspace) return FA_ERR_NULL;
     if (workspace_bytes < ws_need) return FA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % 16) return FA_ERR_ALIGN;
@@ -220,6 +223,17 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
 }
 
 }  // namespace
+
+namespace fa {
+
+int check_splitkv_args(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int Nq, int Nk, int d, const int* seqlens_k, float scale,
+                       int dtype, int num_splits) {
+  return check_forward(q, k, v, o, lse, B, H, Nq, Nk, d, dtype, scale, seqlens_k, num_splits,
+                       nullptr, 0, false, false);
+}
+
+}  // namespace fa
 
 extern "C" {
 

@@ -1,5 +1,6 @@
-// fa_internal.h -- declarations shared by the two translation units of the CUDA library
-// (fa_api.cpp: argument checks, tensor maps, C ABI; fa_fwd_kernel.cu: kernels and launch).
+// fa_internal.h -- declarations shared by the translation units of the CUDA library
+// (fa_api.cpp: argument checks, tensor maps, C ABI; fa_fwd_kernel.cu, fa_bwd_kernel.cu:
+// kernels and launch; fa_noalloc.cu: the entry point with a built-in workspace).
 // Not part of the public ABI (that is include/fa.h).
 #pragma once
 
@@ -64,6 +65,12 @@ struct BwdParams {
   int fp16;
   float scale;
 };
+
+// Every host-side check fa_fwd_splitkv makes except those of its workspace argument: the
+// FA_* code it would return for these arguments (nothing is enqueued).
+int check_splitkv_args(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int Nq, int Nk, int d, const int* seqlens_k, float scale,
+                       int dtype, int num_splits);
 
 // Enqueue the backward (pre-kernel, main kernel, post-kernel).
 cudaError_t launch_bwd(const BwdParams& p, cudaStream_t stream);

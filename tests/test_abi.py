@@ -116,6 +116,32 @@ def test_splitkv_host_side_checks(lib):
     assert lib.fa_error_string(-11) == b"workspace smaller than fa_fwd_splitkv_workspace_size()"
 
 
+def _noalloc(lib, q=0x10000, k=0x20000, v=0x30000, o=0x40000, lse=0x50000, B=1, H=1, Nq=16,
+             Nk=128, d=64, causal=0, wl=-1, wr=-1, lens=None, scale=0.125, dtype=0, splits=2):
+    # Fake, never dereferenced addresses: every case below fails a host-side check first.
+    fn = lib.fa_fwd_splitkv_noalloc
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, f32, i32, i32,
+                   vp]
+    fn.restype = i32
+    return fn(q, k, v, o, lse, B, H, Nq, Nk, d, causal, wl, wr, lens, scale, dtype, splits, None)
+
+
+def test_noalloc_checks_arguments_like_splitkv(lib):
+    """fa_fwd_splitkv_noalloc gives fa_fwd_splitkv's codes for bad arguments, before it looks
+    at its built-in buffer: a split count beyond the limit is a shape error even when its
+    parts would not fit the buffer either."""
+    assert _noalloc(lib, q=0) == FA_ERR_NULL
+    assert _noalloc(lib, splits=129) == FA_ERR_SHAPE
+    assert _noalloc(lib, splits=129, B=64, H=64, Nq=256) == FA_ERR_SHAPE
+    assert _noalloc(lib, splits=0) == FA_ERR_SHAPE
+    assert _noalloc(lib, Nk=8) == FA_ERR_SHAPE
+    assert _noalloc(lib, dtype=5) == FA_ERR_DTYPE
+    assert _noalloc(lib, scale=float("nan")) == FA_ERR_SCALE
+    assert _noalloc(lib, q=0x10008) == FA_ERR_ALIGN
+    assert _noalloc(lib, o=0x10000) == FA_ERR_ALIAS
+
+
 def test_fwd_host_host_side_checks(lib):
     # Fake, never dereferenced addresses: every case below fails a host-side check first.
     h = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000]

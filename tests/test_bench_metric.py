@@ -81,3 +81,18 @@ def test_algorithmic_bytes_and_warm_l2_selection():
              if bench.algorithmic_bytes(x) < bench.WARM_L2_MAX_BYTES}
     assert small == {"tiny_n256_d64", "n1k_d64", "n1k_d64_causal", "n1k_d128"}
     assert bench.WARM_L2_MAX_BYTES < bench.L2_FLUSH_BYTES
+
+
+def test_reference_arm_prints_the_gpu_arms_config(capsys):
+    """The reference arm's JSON line carries exactly the config the GPU arm prints for the same
+    workload (run here on the tiny workload with a bounded oracle sample)."""
+    import json
+    import types
+    w = WORKLOADS["tiny_n256_d64"]
+    args = types.SimpleNamespace(gpus=1, steps=3, warmup=3, ref_total_seconds=0.5)
+    assert bench.run_reference(args, w) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.bench_config(w, 1)
+    import inspect
+    assert "bench_config(w, world)" in inspect.getsource(bench.run_gpu)

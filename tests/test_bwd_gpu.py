@@ -1,25 +1,22 @@
 """Parity of the backward (fa_bwd) with the fp64 oracle's gradients.
 
 The GPU forward provides O and LSE (as a user would run it); the oracle differentiates the exact
-definition on the same bf16/fp16 inputs. Tolerances, derived from the arithmetic: P and dS are
-rounded to the input type before their products (2^-9 relative for bf16), D uses the rounded
-O, and the outputs are rounded to the input type, so each gradient is held to a relative L2
-error of 2e-2 and a largest element error of 5e-2 of its largest element. Where the exact
-gradient vanishes (dQ and dK with a single key), the computed one must stay below 1e-3.
+definition on the same bf16/fp16 inputs. The bar (``oracle.tolerance.grad_bars``) follows from
+the arithmetic: with u the unit roundoff of the input type (2^-8 bf16, 2^-11 fp16), P and dS
+are rounded to the input type before their products, D uses the rounded O and the outputs are
+rounded, so each gradient is held to a relative L2 error of 2u and a largest element error of
+6u of its largest element. Where the exact gradient vanishes (dQ and dK with a single key), the
+computed one must stay below 1e-3.
 """
 import numpy as np
 import pytest
 
 import oracle
-from gpu_util import to_device
+from gpu_util import check_grad, dq_allowance_for, to_device
 from io_aware_attention_fa2_gb300.inputs import (WORKLOADS, make_qkv, make_workload, normal,
                                                  round_to_bits, softmax_scale)
 
 pytestmark = pytest.mark.gpu
-
-REL_L2 = 2e-2
-REL_MAX = 5e-2
-
 
 def run_case(B, H, N, d, dtype, causal, seed):
     import torch
@@ -37,15 +34,10 @@ def run_case(B, H, N, d, dtype, causal, seed):
     assert binding.device_error() == 0
     got = [t.double().cpu().numpy() for t in (dq, dk, dv)]
     ref = oracle.attention_bwd(qb, kb, vb, dob, causal, scale, dtype=dtype)
+    allow = dq_allowance_for(qb, kb, vb, dob, causal, scale, dtype)
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
-        assert np.isfinite(g).all(), name
-        if np.abs(r).max() < 1e-6:
-            # the exact gradient vanishes (e.g. dQ, dK with one key): only rounding is left
-            assert np.abs(g).max() <= 1e-3, (name, float(np.abs(g).max()))
-            continue
-        err = np.linalg.norm(g - r) / np.linalg.norm(r)
-        mx = np.abs(g - r).max() / np.abs(r).max()
-        assert err <= REL_L2 and mx <= REL_MAX, (name, B, H, N, d, dtype, causal, err, mx)
+        check_grad(name, g, r, dtype, (B, H, N, d, dtype, causal),
+                   allow if name == "dq" else None)
 
 
 @pytest.mark.parametrize("N", [1, 17, 128, 200, 257])
@@ -65,6 +57,31 @@ def test_bwd_longer(causal):
     run_case(1, 4, 1024, 128, "bf16", causal, seed=991)
 
 
+@pytest.mark.parametrize("name", ["n1k_d128", "n1k_d64", "n1k_d64_causal"])
+def test_bwd_workload_every_element(name):
+    """The N = 1K workloads (B=2 H=16 d=128 and B=4 H=16 d=64, the latter causal and not) with
+    the bench's upstream gradient, one fa_bwd call as the bench launches it; every element of
+    dQ, dK and dV against the full fp64 gradients."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    w = WORKLOADS[name]
+    qb, kb, vb = make_workload(w)
+    dob = round_to_bits(normal(qb.shape, w.seed + 9), w.dtype)
+    q, k, v, do = (to_device(x, w.dtype) for x in (qb, kb, vb, dob))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, device="cuda")
+    binding.fa_fwd(q, k, v, o, lse, w.causal, w.scale)
+    grads = [torch.full_like(q, float("nan")) for _ in range(3)]
+    binding.fa_bwd(q, k, v, o, do, lse, *grads, w.causal, w.scale)
+    assert binding.device_error() == 0
+    ref = oracle.attention_bwd(qb, kb, vb, dob, w.causal, w.scale, dtype=w.dtype)
+    allow = dq_allowance_for(qb, kb, vb, dob, w.causal, w.scale, w.dtype)
+    for name_g, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        check_grad(name_g, g.double().cpu().numpy(), r, w.dtype, name,
+                   allow if name_g == "dq" else None)
+
+
 def test_bwd_bad_arguments():
     import torch
 
@@ -82,19 +99,26 @@ def test_bwd_bad_arguments():
     assert e.value.code == -5
 
 
-@pytest.mark.parametrize("name,heads", [("n8k_d128_causal", [(0, 3), (1, 12)]),
+ALL_HEADS = "all"
+
+
+@pytest.mark.parametrize("name,heads", [("n8k_d128_causal", ALL_HEADS),
                                         ("n8k_d128", [(1, 7)]),
                                         ("n2000_d128_fp16_stress", [(0, 0), (15, 31)]),
                                         ("n1k_d64_causal", [(3, 15)])])
 def test_bwd_full_size_sampled(name, heads):
-    """Full-size workloads (the benchmarked B=2, H=16, N=8192, d=128 bf16 shape, the fp16 stress
-    shape with its large logits, d=64) with the bench's upstream gradient, one fa_bwd call as
-    the bench launches it; dQ, dK, dV compared on sampled positions (tile edges, the middle,
-    the last row and seeded ones) of the given heads against the sampled fp64 oracle."""
+    """Full-size workloads (the benchmarked B=2, H=16, N=8192, d=128 bf16 shape -- every one of
+    its 32 heads --, the fp16 stress shape with its large logits, d=64) with the bench's
+    upstream gradient, one fa_bwd call as the bench launches it; dQ, dK, dV compared on sampled
+    positions against the sampled fp64 oracle: both sides of every 128-row tile edge near the
+    start, middle and end (the causal diagonal of a key block runs through its own Q tile),
+    the last row, and seeded ones."""
     import torch
 
     from io_aware_attention_fa2_gb300 import binding
     w = WORKLOADS[name]
+    if heads == ALL_HEADS:
+        heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     qb, kb, vb = make_workload(w)
     dob = round_to_bits(normal(qb.shape, w.seed + 9), w.dtype)
     q, k, v, do = (to_device(x, w.dtype) for x in (qb, kb, vb, dob))
@@ -104,19 +128,22 @@ def test_bwd_full_size_sampled(name, heads):
     dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
     binding.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale)
     assert binding.device_error() == 0
-    pos = np.unique(np.concatenate([[0, 1, 127, 128, 129, w.N // 2, w.N - 128, w.N - 1],
+    mid = (w.N // 2) // 128 * 128
+    edges = [0, 1, 127, 128, 129, 255, 256, mid - 1, mid, mid + 127, w.N - 129, w.N - 128,
+             w.N - 1]
+    pos = np.unique(np.concatenate([[p for p in edges if 0 <= p < w.N],
                                     np.random.default_rng(w.seed + 17).integers(0, w.N, 8)]))
     ref = oracle.attention_bwd_sampled(qb, kb, vb, dob, w.causal, w.scale, heads, pos, pos,
                                        dtype=w.dtype)
+    rows = [(b, h, i) for b, h in heads for i in pos]
+    allow = dq_allowance_for(qb, kb, vb, dob, w.causal, w.scale, w.dtype, rows)
+    allow = allow.reshape(len(heads), len(pos), -1)
     sel = torch.from_numpy(pos).cuda()
     for t, (b, h) in enumerate(heads):
         for name_g, g_all, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
             g = g_all[b, sel, h].double().cpu().numpy()
-            r = r[t]
-            assert np.isfinite(g).all(), name_g
-            err = np.linalg.norm(g - r) / np.linalg.norm(r)
-            mx = np.abs(g - r).max() / np.abs(r).max()
-            assert err <= REL_L2 and mx <= REL_MAX, (name, b, h, name_g, err, mx)
+            check_grad(name_g, g, r[t], w.dtype, (name, b, h),
+                       allow[t] if name_g == "dq" else None)
 
 
 @pytest.mark.parametrize("B,H,N,d,causal,pinned", [
@@ -212,6 +239,8 @@ def run_masked_case(B, H, N, d, causal, window, lens, seed):
     got = [t.double().cpu().numpy() for t in (dq, dk, dv)]
     ref = oracle.attention_bwd(qb, kb, vb, dob, causal, scale, dtype="bf16", window=window,
                                seqlens_k=lens)
+    allow = dq_allowance_for(qb, kb, vb, dob, causal, scale, "bf16", window=window,
+                             seqlens_k=lens)
     what = (B, H, N, d, causal, window, lens)
     # keys past a batch's key length have no query, and a batch with no key has no gradient
     # at all: exactly zero on the GPU as well
@@ -220,13 +249,7 @@ def run_masked_case(B, H, N, d, causal, window, lens, seed):
         if n == 0:
             assert not got[0][b].any(), what
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
-        assert np.isfinite(g).all(), (name, what)
-        if np.abs(r).max() < 1e-6:
-            assert np.abs(g).max() <= 1e-3, (name, what, float(np.abs(g).max()))
-            continue
-        err = np.linalg.norm(g - r) / np.linalg.norm(r)
-        mx = np.abs(g - r).max() / np.abs(r).max()
-        assert err <= REL_L2 and mx <= REL_MAX, (name, what, err, mx)
+        check_grad(name, g, r, "bf16", what, allow if name == "dq" else None)
 
 
 MASKS = [((64, 0), None), ((100, 30), None), ((0, 0), None), ((-1, -1), "third"),
@@ -273,17 +296,17 @@ def test_bwd_masked_full_size_sampled(name, heads):
                                     np.random.default_rng(w.seed + 17).integers(0, w.N, 8)]))
     ref = oracle.attention_bwd_sampled(qb, kb, vb, dob, w.causal, w.scale, heads, pos, pos,
                                        dtype=w.dtype, window=w.window, seqlens_k=lens)
+    rows = [(b, h, i) for b, h in heads for i in pos]
+    allow = dq_allowance_for(qb, kb, vb, dob, w.causal, w.scale, w.dtype, rows, w.window, lens)
+    allow = allow.reshape(len(heads), len(pos), -1)
     sel = torch.from_numpy(pos).cuda()
     for t, (b, h) in enumerate(heads):
         for name_g, g_all, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
             g = g_all[b, sel, h].double().cpu().numpy()
-            r = r[t]
-            assert np.isfinite(g).all(), name_g
             if lens and name_g != "dq":
                 assert not g[pos >= lens[b]].any(), (name, b, h, name_g)
-            err = np.linalg.norm(g - r) / np.linalg.norm(r)
-            mx = np.abs(g - r).max() / np.abs(r).max()
-            assert err <= REL_L2 and mx <= REL_MAX, (name, b, h, name_g, err, mx)
+            check_grad(name_g, g, r[t], w.dtype, (name, b, h),
+                       allow[t] if name_g == "dq" else None)
 
 
 def test_bwd_masked_host_path_matches_device_path():
@@ -335,13 +358,15 @@ def test_bwd_partial_dispatch_group():
     pos = np.array([0, 1, 127, 128, 4095, 4096, 8063, 8064, 8191])
     ref = oracle.attention_bwd_sampled(qb, kb, vb, dob, True, scale, heads, pos, pos,
                                        dtype="bf16")
+    rows = [(b, h, i) for b, h in heads for i in pos]
+    allow = dq_allowance_for(qb, kb, vb, dob, True, scale, "bf16", rows)
+    allow = allow.reshape(len(heads), len(pos), -1)
     sel = torch.from_numpy(pos).cuda()
     for t, (b, h) in enumerate(heads):
         for name, g_all, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
             g = g_all[b, sel, h].double().cpu().numpy()
-            err = np.linalg.norm(g - r[t]) / np.linalg.norm(r[t])
-            mx = np.abs(g - r[t]).max() / np.abs(r[t]).max()
-            assert err <= REL_L2 and mx <= REL_MAX, (h, name, err, mx)
+            check_grad(name, g, r[t], "bf16", ("H=11 groups", h),
+                       allow[t] if name == "dq" else None)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -365,11 +390,11 @@ def test_bwd_masks_fp16(causal):
     assert binding.device_error() == 0
     ref = oracle.attention_bwd(qb, kb, vb, dob, causal, scale, dtype="fp16", window=window,
                                seqlens_k=lens)
+    allow = dq_allowance_for(qb, kb, vb, dob, causal, scale, "fp16", window=window,
+                             seqlens_k=lens)
     for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
-        g = g.double().cpu().numpy()
-        err = np.linalg.norm(g - r) / np.linalg.norm(r)
-        mx = np.abs(g - r).max() / np.abs(r).max()
-        assert err <= REL_L2 and mx <= REL_MAX, (name, causal, err, mx)
+        check_grad(name, g.double().cpu().numpy(), r, "fp16", ("masked fp16", causal),
+                   allow if name == "dq" else None)
 
 
 @pytest.mark.parametrize("scale", [0.0, -0.09, 1.0])
@@ -391,12 +416,7 @@ def test_bwd_scale_values(scale, causal):
     binding.fa_bwd(q, k, v, o, do, lse, *grads, causal, scale)
     assert binding.device_error() == 0
     ref = oracle.attention_bwd(qb, kb, vb, dob, causal, scale, dtype="bf16")
+    allow = dq_allowance_for(qb, kb, vb, dob, causal, scale, "bf16")
     for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
-        g = g.double().cpu().numpy()
-        assert np.isfinite(g).all(), name
-        if np.abs(r).max() < 1e-6:
-            assert np.abs(g).max() <= 1e-3, (name, scale, float(np.abs(g).max()))
-            continue
-        err = np.linalg.norm(g - r) / np.linalg.norm(r)
-        mx = np.abs(g - r).max() / np.abs(r).max()
-        assert err <= REL_L2 and mx <= REL_MAX, (name, scale, causal, err, mx)
+        check_grad(name, g.double().cpu().numpy(), r, "bf16", ("scale", scale, causal),
+                   allow if name == "dq" else None)

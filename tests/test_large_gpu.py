@@ -12,7 +12,8 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_util import MAX_ABS_LSE, MAX_ABS_O, REL_L2_O, to_device
+from gpu_util import (MAX_ABS_LSE, REL_L2_O, check_grad, dq_allowance_for, o_bound,
+                      to_device)
 from io_aware_attention_fa2_gb300.inputs import make_qkv, normal, round_to_bits, softmax_scale
 
 pytestmark = pytest.mark.gpu
@@ -39,7 +40,7 @@ def _heads_past_2_31(B, N, H, d):
 def _check(o, lse, o_ref, lse_ref, what):
     assert np.isfinite(o).all() and np.isfinite(lse).all(), what
     d_o = o - o_ref
-    assert np.abs(d_o).max() <= MAX_ABS_O, (what, float(np.abs(d_o).max()))
+    assert (np.abs(d_o) - o_bound(o_ref, "bf16")).max() <= 0, (what, float(np.abs(d_o).max()))
     assert np.linalg.norm(d_o) / np.linalg.norm(o_ref) <= REL_L2_O, what
     assert np.abs(lse - lse_ref).max() <= MAX_ABS_LSE, what
 
@@ -77,12 +78,11 @@ def test_forward_and_backward_past_2_31_elements():
     assert binding.device_error() == 0
     for (b, h), (qb, kb, vb, dob) in small.items():
         refs = oracle.attention_bwd(qb, kb, vb, dob, True, scale, dtype="bf16")
+        allow = dq_allowance_for(qb, kb, vb, dob, True, scale, "bf16")
         for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
             got = g[b, :, h, :].double().cpu().numpy()[None, :, None, :]
-            assert np.isfinite(got).all(), (name, b, h)
-            err = np.linalg.norm(got - r) / np.linalg.norm(r)
-            mx = np.abs(got - r).max() / np.abs(r).max()
-            assert err <= 2e-2 and mx <= 5e-2, (name, b, h, err, mx)
+            check_grad(name, got, r, "bf16", ("past 2^31", b, h),
+                       allow if name == "dq" else None)
     del q, k, v, do, o, lse, dq, dk, dv
     torch.cuda.empty_cache()
 

@@ -5,14 +5,16 @@ instead of a caller workspace.
 
 Checked through the C ABI against fa_fwd_splitkv with a workspace PyTorch allocates, on two
 calls in a row: the second call has a different shape and reuses the buffer the first one left
-behind. This file is collected last so that a run stopping at the first failure has run every
-other test before it; it also passes alone in a fresh process.
+behind. Both run the same kernels on the same values, so the outputs must be bit-identical.
+A further check makes several calls and reads the device's free memory before and after: a
+call that allocated would lower it. This file is collected last so that a run stopping at the
+first failure has run every other test before it; it also passes alone in a fresh process.
 """
 import ctypes
 
 import pytest
 
-from gpu_util import MAX_ABS_LSE, MAX_ABS_O, to_device
+from gpu_util import to_device
 from io_aware_attention_fa2_gb300.inputs import make_qkv, softmax_scale
 
 pytestmark = pytest.mark.gpu
@@ -64,8 +66,29 @@ def test_two_calls_match_splitkv_with_own_workspace():
         torch.cuda.synchronize()
         assert binding.device_error() == 0
         assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
-        assert (o.float() - o_ref.float()).abs().max().item() <= MAX_ABS_O
-        assert (lse - lse_ref).abs().max().item() <= MAX_ABS_LSE
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(lse, lse_ref)
+
+
+def test_calls_allocate_no_device_memory():
+    import torch
+
+    from io_aware_attention_fa2_gb300 import binding
+    lib = _lib()
+    B, H, Nq, Nk, d, splits = 1, 8, 2, 8192, 128, 8
+    qb, kb, vb = make_qkv(B, H, Nq, d, "bf16", 903, Nk=Nk)
+    q, k, v = (to_device(x, "bf16") for x in (qb, kb, vb))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Nq, device="cuda")
+    assert _call_noalloc(lib, q, k, v, o, lse, True, splits) == 0      # set-up done here
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(8):
+        assert _call_noalloc(lib, q, k, v, o, lse, True, splits) == 0
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert binding.device_error() == 0
+    assert free_after >= free_before, (free_before, free_after)
 
 
 def test_parts_beyond_the_buffer_are_rejected():
