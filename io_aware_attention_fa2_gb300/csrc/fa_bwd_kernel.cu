@@ -381,24 +381,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                           : ptx::idesc_f16(FP16, BLOCK_M, D, true, true);
       auto qbase = [&](int n) { return sQ + (n % kBwdStages) * L::kTile; };
       auto dobase = [&](int n) { return sdO + (n % kBwdStages) * L::kTile; };
+      // Descriptors of the operands' bases: K-major (LBO 16) and MN-major (LBO = next box).
+      const ptx::SmemDesc k_kmaj = ptx::smem_desc_sw128_split(sK, 16, 1024);
+      const ptx::SmemDesc v_kmaj = ptx::smem_desc_sw128_split(sV, 16, 1024);
+      const ptx::SmemDesc k_mn = ptx::smem_desc_sw128_split(sK, kBoxBytes, 1024);
+      const ptx::SmemDesc ds_mn = ptx::smem_desc_sw128_split(sdS, kBoxBytes, 1024);
+      const ptx::SmemDesc ds_kmaj = ptx::smem_desc_sw128_split(sdS, 16, 1024);
       // S^T = K_j Q_i^T -> T_S and dP^T = V_j dO_i^T -> T_dP: both operands K-major over d.
       auto issue_s = [&](int n) {
         ptx::tc_fence_after_sync();
+        const ptx::SmemDesc q_desc = ptx::smem_desc_sw128_split(qbase(n), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-          ptx::mma_f16_ss(tmem + kT_S, ptx::smem_desc_sw128(sK + off, 16, 1024),
-                          ptx::smem_desc_sw128(qbase(n) + off, 16, 1024), id_st, kk > 0);
+          ptx::mma_f16_ss(tmem + kT_S, k_kmaj.at(off), q_desc.at(off), id_st, kk > 0);
         }
         ptx::mma_commit(bar(BB_S_FULL));
       };
       auto issue_dp = [&](int n) {
         ptx::tc_fence_after_sync();
+        const ptx::SmemDesc do_desc = ptx::smem_desc_sw128_split(dobase(n), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-          ptx::mma_f16_ss(tmem + kT_dP, ptx::smem_desc_sw128(sV + off, 16, 1024),
-                          ptx::smem_desc_sw128(dobase(n) + off, 16, 1024), id_st, kk > 0);
+          ptx::mma_f16_ss(tmem + kT_dP, v_kmaj.at(off), do_desc.at(off), id_st, kk > 0);
         }
         ptx::mma_commit(bar(BB_DP_FULL));
       };
@@ -414,11 +420,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // d contiguous (MN-major): 16 query rows of 128 bytes per MMA, LBO = next 64 columns.
         if (!wait(BB_P_FULL, n & 1)) { ok = false; break; }
         ptx::tc_fence_after_sync();
+        const ptx::SmemDesc do_mn = ptx::smem_desc_sw128_split(dobase(n), kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < BLOCK_M / 16; ++kk)
-          ptx::mma_f16_ts(tmem + kT_dV, tmem + kT_S + kk * 8,
-                          ptx::smem_desc_sw128(dobase(n) + kk * 16 * 128, kBoxBytes, 1024),
-                          id_acc, (n > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_f16_ts(tmem + kT_dV, tmem + kT_S + kk * 8, do_mn.at(kk * 16 * 128), id_acc,
+                          (n > 0 || kk > 0) ? 1u : 0u);
         if (!wait(BB_DS_FULL, n & 1)) { ok = false; break; }
         // S^T(i+1) over P^T(i): the softmax warps have read P^T(i) back for dS(i), and dV(i),
         // issued before, reads it first (in-order pipe).
@@ -435,8 +441,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // MMA: the dS' rows (queries contiguous) and K_j (d contiguous).
 #pragma unroll
         for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
-          const uint64_t ds_desc = ptx::smem_desc_sw128(sdS + kk * 16 * 128, kBoxBytes, 1024);
-          const uint64_t k_desc = ptx::smem_desc_sw128(sK + kk * 16 * 128, kBoxBytes, 1024);
+          const uint64_t ds_desc = ds_mn.at(kk * 16 * 128);
+          const uint64_t k_desc = k_mn.at(kk * 16 * 128);
           if constexpr (D == 128)
             ptx::mma_f16_ss(tmem + kT_dP, k_desc, ds_desc, id_dq, kk > 0);
           else
@@ -445,13 +451,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::mma_commit(bar(BB_DQ_FULL));
         // dK += dS'^T Q_i: A = the same dS' rows read K-major (queries are the K dimension),
         // B = Q_i MN-major.
+        const ptx::SmemDesc q_mn = ptx::smem_desc_sw128_split(qbase(n), kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < BLOCK_M / 16; ++kk)
-          ptx::mma_f16_ss(tmem + kT_dV + D,
-                          ptx::smem_desc_sw128(sdS + (kk / 4) * kBoxBytes + (kk % 4) * 32, 16,
-                                               1024),
-                          ptx::smem_desc_sw128(qbase(n) + kk * 16 * 128, kBoxBytes, 1024),
-                          id_acc, (n > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_f16_ss(tmem + kT_dV + D, ds_kmaj.at((kk / 4) * kBoxBytes + (kk % 4) * 32),
+                          q_mn.at(kk * 16 * 128), id_acc, (n > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar(BB_QD_EMPTY + s));   // Q_i and dO_i are no longer read
         // dP^T(i+1) over dQ(i) once the dQ warps have read it out.
         if (next) {

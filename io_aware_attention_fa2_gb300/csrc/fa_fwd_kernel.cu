@@ -301,15 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_x(j) = Q_x K_j^T into the S columns of tile x (K_j sits in stage (j - u0) % kStages).
       auto issue_s = [&](int x, int j) {
         ptx::tc_fence_after_sync();
-        const uint32_t q_base = sQ + x * L::kTile;
-        const uint32_t k_base = sK + ((j - u0) % kStages) * L::kTile;
+        const ptx::SmemDesc q_desc = ptx::smem_desc_sw128_split(sQ + x * L::kTile, 16, 1024);
+        const ptx::SmemDesc k_desc =
+            ptx::smem_desc_sw128_split(sK + ((j - u0) % kStages) * L::kTile, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // 16 elements (32 bytes) of d per MMA: 4 steps inside one 128-byte swizzle span,
           // then the next 64-column box.
           const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-          ptx::mma_f16_ss(tmem + x * BLOCK_N, ptx::smem_desc_sw128(q_base + off, 16, 1024),
-                          ptx::smem_desc_sw128(k_base + off, 16, 1024), idesc_qk, kk > 0);
+          ptx::mma_f16_ss(tmem + x * BLOCK_N, q_desc.at(off), k_desc.at(off), idesc_qk, kk > 0);
         }
         ptx::mma_commit(bar(BAR_S_FULL + x));
       };
@@ -318,12 +318,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The first P V of a tile overwrites O instead of accumulating.
       auto issue_pv = [&](int x, int j, bool first) {
         ptx::tc_fence_after_sync();
-        const uint32_t v_base = sV + ((j - u0) % kStages) * L::kTile;
+        const ptx::SmemDesc v_desc =
+            ptx::smem_desc_sw128_split(sV + ((j - u0) % kStages) * L::kTile, kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < BLOCK_N / 16; ++kk)
           ptx::mma_f16_ts(tmem + kTmemO + x * D, tmem + x * BLOCK_N + kk * 8,
-                          ptx::smem_desc_sw128(v_base + kk * 16 * 128, kBoxBytes, 1024),
-                          idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                          v_desc.at(kk * 16 * 128), idesc_pv, (!first || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar(BAR_O_DONE + x));
       };
 

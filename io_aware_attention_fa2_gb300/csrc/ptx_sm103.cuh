@@ -217,6 +217,26 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The same descriptor kept as its two 32-bit words, for operands at base + off: with off a
+// multiple of 16 bytes and every address below 256 KiB, the descriptor of base + off has the
+// same high word and a low word larger by off / 16 (the 14-bit start-address field cannot
+// carry into the leading-dimension offset). Building each MMA's descriptor is then one 32-bit
+// add, which keeps the single MMA-issuing thread's instruction stream short.
+struct SmemDesc {
+  uint32_t lo, hi;
+  __device__ __forceinline__ uint64_t at(uint32_t off) const {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo + (off >> 4)), "r"(hi));
+    return d;
+  }
+};
+
+__device__ __forceinline__ SmemDesc smem_desc_sw128_split(uint32_t saddr, uint32_t lbo_bytes,
+                                                          uint32_t sbo_bytes) {
+  const uint64_t d = smem_desc_sw128(saddr, lbo_bytes, sbo_bytes);
+  return SmemDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+
 // Instruction descriptor for kind::f16 (32 bit): D format f32 (1) in [4,6); A and B formats
 // in [7,10) and [10,13) (0 = f16, 1 = bf16); A / B major-ness in bits 15 / 16 (0 = K-major,
 // 1 = MN-major); N >> 3 in [17,23); M >> 4 in [24,29).
