@@ -57,20 +57,31 @@ __device__ int g_device_error = 0;
 namespace {
 
 constexpr int kStages = 2;                     // depth of the K ring and of the V ring
-constexpr int kThreads = 320;                  // 10 warps
-constexpr int kQTiles = 2;                     // 128-row Q tiles per CTA
+constexpr int kMaxQTiles = 2;                  // 128-row Q tiles per CTA: 2, or 1 (see Cfg)
 constexpr uint32_t kBoxBytes = BOX_ROWS * BOX_COLS * 2;   // 16 KiB
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;          // 1 s per wait
 constexpr int kErrTimeout = -8;                            // FA_ERR_TIMEOUT
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int D>
+// Shape of one CTA. QT = 2: two Q tiles (A, B) whose softmax phases alternate on the tensor
+// pipe; 512 TMEM columns (S_A, S_B, O_A, O_B), one CTA per SM. QT = 1 (d = 64 only): one Q
+// tile, S 128 + O 64 columns in a 256-column allocation, 6 warps and 80 KiB of shared memory,
+// so that two CTAs share an SM and one's start and end overlap the other's main loop.
+template <int QT, int D>
+struct Cfg {
+  static constexpr int kQTiles = QT;
+  static constexpr int kThreads = 64 + 128 * QT;
+  static constexpr int kMinBlocks = QT == 2 ? 1 : 2;
+  static constexpr uint32_t kTmemO = 128 * QT;                     // O_X at kTmemO + x * D
+  static constexpr uint32_t kTmemCols = QT == 2 ? 512 : 256;
+  static_assert(kTmemO + QT * D <= kTmemCols, "TMEM columns");
+};
+
+template <int QT, int D>
 struct SmemLayout {
   static constexpr uint32_t kTile = (D / BOX_COLS) * kBoxBytes;    // one Q, K or V tile
-  static constexpr uint32_t kQ = 0;                                 // Q_A, Q_B
-  static constexpr uint32_t kK = kQ + kQTiles * kTile;
+  static constexpr uint32_t kQ = 0;                                 // Q_A (, Q_B)
+  static constexpr uint32_t kK = kQ + QT * kTile;
   static constexpr uint32_t kV = kK + kStages * kTile;
   static constexpr uint32_t kBars = kV + kStages * kTile;
   static constexpr uint32_t kNumBars = 24;
@@ -86,9 +97,9 @@ enum : int {
   BAR_V_FULL = BAR_K_EMPTY + kStages,     // + stage
   BAR_V_EMPTY = BAR_V_FULL + kStages,     // + stage
   BAR_S_FULL = BAR_V_EMPTY + kStages,     // + tile: S_X(j) computed (and all earlier MMAs)
-  BAR_P_FULL = BAR_S_FULL + kQTiles,      // + tile: P_X(j) in TMEM, O_X rescaled (128 arrivals)
-  BAR_O_DONE = BAR_P_FULL + kQTiles,      // + tile: P_X(j) V_j computed
-  BAR_MMA_DONE = BAR_O_DONE + kQTiles,
+  BAR_P_FULL = BAR_S_FULL + kMaxQTiles,   // + tile: P_X(j) in TMEM, O_X rescaled (128 arrivals)
+  BAR_O_DONE = BAR_P_FULL + kMaxQTiles,   // + tile: P_X(j) V_j computed
+  BAR_MMA_DONE = BAR_O_DONE + kMaxQTiles,
   BAR_COUNT = BAR_MMA_DONE + 1
 };
 static_assert(BAR_COUNT <= 24, "barrier slots");
@@ -150,8 +161,8 @@ struct KeyMask {
 };
 
 // ---------------------------------------------------------------------------------------------
-template <int D, bool FP16, bool WINDOWED>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int QT, int D, bool FP16, bool WINDOWED>
+__global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlocks))
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
@@ -159,7 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float scale_log2, int heads_per_group, int window_left, int window_right,
                   const int* __restrict__ seqlens_k, int num_splits,
                   float* __restrict__ o_part, float* __restrict__ lse_part) {
-  using L = SmemLayout<D>;
+  using L = SmemLayout<QT, D>;
+  using C = Cfg<QT, D>;
+  constexpr int kQTiles = QT;
+  constexpr uint32_t kTmemO = C::kTmemO;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
@@ -200,7 +214,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a1 <= b1 when both are non-empty) and their union [u0, u1), which the producer streams.
   int a0, a1, b0, b1;
   mask.tile_range(kQTiles * qblk, Nq, a0, a1);
-  mask.tile_range(kQTiles * qblk + 1, Nq, b0, b1);
+  if constexpr (QT == 2) {
+    mask.tile_range(kQTiles * qblk + 1, Nq, b0, b1);
+  } else {
+    b0 = b1 = 0;   // no tile B
+  }
   if (num_splits > 1) {
     // this CTA's part of the block's K/V tiles: [c0, c1)
     const int w0 = a1 > a0 ? a0 : b0, w1 = b1 > b0 ? b1 : a1;
@@ -234,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_barrier_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(&tmem_base_slot), kTmemCols);
+    ptx::tmem_alloc(ptx::smem_addr(&tmem_base_slot), C::kTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before_sync();
@@ -328,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       auto on_a = [&](int j) { return a0 <= j && j < a1; };
-      auto on_b = [&](int j) { return b0 <= j && j < b1; };
+      auto on_b = [&](int j) { return QT == 2 && b0 <= j && j < b1; };
       // K_j / V_j are load number j - u0 of the sequence.
       auto wait_k = [&](int j) {
         return wait(BAR_K_FULL + (j - u0) % kStages, ((j - u0) / kStages) & 1);
@@ -570,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after_sync();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -621,21 +639,21 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) lse_ptr[row] = lse_row;
 }
 
-template <int D, bool FP16, bool WINDOWED>
+template <int QT, int D, bool FP16, bool WINDOWED>
 cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
-  auto kernel = fa_fwd_kernel<D, FP16, WINDOWED>;
-  const size_t smem = SmemLayout<D>::kDynamic;
+  auto kernel = fa_fwd_kernel<QT, D, FP16, WINDOWED>;
+  const size_t smem = SmemLayout<QT, D>::kDynamic;
   cudaError_t err =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  const long long num_qblk = (p.Nq + kQTiles * BLOCK_M - 1) / (kQTiles * BLOCK_M);
+  const long long num_qblk = (p.Nq + QT * BLOCK_M - 1) / (QT * BLOCK_M);
   const long long bh = static_cast<long long>(p.B) * p.H;
   const dim3 grid(static_cast<unsigned>(num_qblk * bh * p.num_splits));
   // Heads per dispatch group: K and V of a group within ~64 MiB of L2.
   const long long kv_bytes_per_head = 4ll * p.Nk * p.d;
   const int heads_per_group =
       static_cast<int>(std::max(1ll, std::min(bh, (64ll << 20) / kv_bytes_per_head)));
-  kernel<<<grid, kThreads, smem, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.o, p.lse, p.H, p.Nq, p.Nk,
+  kernel<<<grid, Cfg<QT, D>::kThreads, smem, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.o, p.lse, p.H, p.Nq, p.Nk,
                                            p.causal, p.scale_log2, heads_per_group,
                                            p.window_left, p.window_right, p.seqlens_k,
                                            p.num_splits, p.o_part, p.lse_part);
@@ -649,13 +667,22 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+// Sequences up to this many queries use one Q tile per CTA at d = 64 (two CTAs per SM).
+// Measured at B=4, H=16, N=1024: causal 32.7 -> 30.2 us, non-causal unchanged; at N = 2048
+// and longer the two-tile CTA is as fast or faster.
+constexpr int kOneTileMaxNq = 1024;
+
 template <bool WINDOWED>
 cudaError_t launch_dtype(const FwdParams& p, cudaStream_t stream) {
-  if (p.d == 64)
-    return p.fp16 ? launch_impl<64, true, WINDOWED>(p, stream)
-                  : launch_impl<64, false, WINDOWED>(p, stream);
-  return p.fp16 ? launch_impl<128, true, WINDOWED>(p, stream)
-                : launch_impl<128, false, WINDOWED>(p, stream);
+  if (p.d == 64) {
+    if (p.num_splits == 1 && p.Nq <= kOneTileMaxNq)
+      return p.fp16 ? launch_impl<1, 64, true, WINDOWED>(p, stream)
+                    : launch_impl<1, 64, false, WINDOWED>(p, stream);
+    return p.fp16 ? launch_impl<2, 64, true, WINDOWED>(p, stream)
+                  : launch_impl<2, 64, false, WINDOWED>(p, stream);
+  }
+  return p.fp16 ? launch_impl<2, 128, true, WINDOWED>(p, stream)
+                : launch_impl<2, 128, false, WINDOWED>(p, stream);
 }
 
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
