@@ -69,7 +69,6 @@ constexpr float kRescaleLog2 = 8.0f;
 // so that two CTAs share an SM and one's start and end overlap the other's main loop.
 template <int QT, int D>
 struct Cfg {
-  static constexpr int kQTiles = QT;
   static constexpr int kThreads = 64 + 128 * QT;
   static constexpr int kMinBlocks = QT == 2 ? 1 : 2;
   static constexpr uint32_t kTmemO = 128 * QT;                     // O_X at kTmemO + x * D
