@@ -198,7 +198,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   fa::FwdParams p;
   const bool fp16 = dtype == FA_FP16;
   if (!encode_bnhd(&p.tm_q, q, B, H, Nq, d, fp16) || !encode_bnhd(&p.tm_k, k, B, H, Nk, d, fp16) ||
-      !encode_bnhd(&p.tm_v, v, B, H, Nk, d, fp16))
+      !encode_bnhd(&p.tm_v, v, B, H, Nk, d, fp16) || !encode_bnhd(&p.tm_o, o, B, H, Nq, d, fp16))
     return FA_ERR_CUDA;
   p.o = o;
   p.lse = lse;

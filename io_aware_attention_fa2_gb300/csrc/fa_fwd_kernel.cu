@@ -99,7 +99,8 @@ enum : int {
   BAR_P_FULL = BAR_S_FULL + kMaxQTiles,   // + tile: P_X(j) in TMEM, O_X rescaled (128 arrivals)
   BAR_O_DONE = BAR_P_FULL + kMaxQTiles,   // + tile: P_X(j) V_j computed
   BAR_MMA_DONE = BAR_O_DONE + kMaxQTiles,
-  BAR_COUNT = BAR_MMA_DONE + 1
+  BAR_O_STAGED = BAR_MMA_DONE + 1,        // + tile: the tile's O rows are in shared memory
+  BAR_COUNT = BAR_O_STAGED + kMaxQTiles
 };
 static_assert(BAR_COUNT <= 24, "barrier slots");
 
@@ -164,7 +165,8 @@ template <int QT, int D, bool FP16, bool WINDOWED>
 __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlocks))
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
+                  const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_o, void* __restrict__ o_ptr,
                   float* __restrict__ lse_ptr, int H, int Nq, int Nk, int causal,
                   float scale_log2, int heads_per_group, int window_left, int window_right,
                   const int* __restrict__ seqlens_k, int num_splits,
@@ -246,6 +248,7 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
       ptx::mbar_init(bar(BAR_S_FULL + x), 1);
       ptx::mbar_init(bar(BAR_P_FULL + x), 128);
       ptx::mbar_init(bar(BAR_O_DONE + x), 1);
+      ptx::mbar_init(bar(BAR_O_STAGED + x), 128);
     }
     ptx::mbar_init(bar(BAR_MMA_DONE), 1);
     ptx::fence_barrier_init();
@@ -268,6 +271,7 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
       ptx::prefetch_tensormap(&tm_q);
       ptx::prefetch_tensormap(&tm_k);
       ptx::prefetch_tensormap(&tm_v);
+      ptx::prefetch_tensormap(&tm_o);
       ptx::mbar_arrive_expect_tx(bar(BAR_Q_FULL), kQTiles * L::kTile);
       for (int x = 0; x < kQTiles; ++x)
         for (int c = 0; c < D / BOX_COLS; ++c)
@@ -539,26 +543,32 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
                                        kWaitLimitNs)) {
       ptx::tc_fence_after_sync();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      // One split: the normalised O row goes into tile x's Q buffer (no MMA reads it any more:
+      // its last S finished before the last P V), laid out as the TMA boxes of the O tensor
+      // map (128-byte swizzle: 16-byte chunk k of row r at chunk k ^ (r % 8)); one thread then
+      // stores the whole 128-row tile with TMA, which leaves out rows at or past Nq.
+      const uint32_t staging = sQ + x * L::kTile;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t orr[32];
         ptx::tmem_ld_32x32b_x32(tO + c * 32, orr);
         ptx::tmem_wait_ld();
         ptx::reg_fence(orr);
-        if (valid && num_splits == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(out_row + c * 32);
+        if (num_splits == 1) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
-            uint4 v;
-            v.x = pack2<FP16>(__uint_as_float(orr[8 * t + 0]) * inv_l,
-                              __uint_as_float(orr[8 * t + 1]) * inv_l);
-            v.y = pack2<FP16>(__uint_as_float(orr[8 * t + 2]) * inv_l,
-                              __uint_as_float(orr[8 * t + 3]) * inv_l);
-            v.z = pack2<FP16>(__uint_as_float(orr[8 * t + 4]) * inv_l,
-                              __uint_as_float(orr[8 * t + 5]) * inv_l);
-            v.w = pack2<FP16>(__uint_as_float(orr[8 * t + 6]) * inv_l,
-                              __uint_as_float(orr[8 * t + 7]) * inv_l);
-            dst[t] = v;
+            const int col0 = c * 32 + t * 8;
+            const uint32_t addr = staging + (col0 / BOX_COLS) * kBoxBytes + row * 128 +
+                                  ((((col0 % BOX_COLS) / 8) ^ (row & 7)) << 4);
+            ptx::st_shared_v4(addr,
+                              pack2<FP16>(__uint_as_float(orr[8 * t + 0]) * inv_l,
+                                          __uint_as_float(orr[8 * t + 1]) * inv_l),
+                              pack2<FP16>(__uint_as_float(orr[8 * t + 2]) * inv_l,
+                                          __uint_as_float(orr[8 * t + 3]) * inv_l),
+                              pack2<FP16>(__uint_as_float(orr[8 * t + 4]) * inv_l,
+                                          __uint_as_float(orr[8 * t + 5]) * inv_l),
+                              pack2<FP16>(__uint_as_float(orr[8 * t + 6]) * inv_l,
+                                          __uint_as_float(orr[8 * t + 7]) * inv_l));
           }
         } else if (valid) {
           float4* dst = reinterpret_cast<float4*>(o_part + part_row * D + c * 32);
@@ -568,6 +578,22 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
                                  __uint_as_float(orr[4 * t + 1]) * inv_l,
                                  __uint_as_float(orr[4 * t + 2]) * inv_l,
                                  __uint_as_float(orr[4 * t + 3]) * inv_l);
+        }
+      }
+      if (num_splits == 1) {
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bar(BAR_O_STAGED + x));
+        if (row == 0) {
+          if (ptx::wait_bounded(bar(BAR_O_STAGED + x), 0, abort_p, kWaitLimitNs)) {
+#pragma unroll
+            for (int bx = 0; bx < D / BOX_COLS; ++bx)
+              ptx::tma_store_4d(&tm_o, staging + bx * kBoxBytes, bx * BOX_COLS, h, qt * BLOCK_M,
+                                b);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read0();   // shared memory stays valid until it has been read
+          } else {
+            record_timeout(abort_p);
+          }
         }
       }
       if (valid) {
@@ -652,7 +678,7 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   const long long kv_bytes_per_head = 4ll * p.Nk * p.d;
   const int heads_per_group =
       static_cast<int>(std::max(1ll, std::min(bh, (64ll << 20) / kv_bytes_per_head)));
-  kernel<<<grid, Cfg<QT, D>::kThreads, smem, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.o, p.lse, p.H, p.Nq, p.Nk,
+  kernel<<<grid, Cfg<QT, D>::kThreads, smem, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.tm_o, p.o, p.lse, p.H, p.Nq, p.Nk,
                                            p.causal, p.scale_log2, heads_per_group,
                                            p.window_left, p.window_right, p.seqlens_k,
                                            p.num_splits, p.o_part, p.lse_part);

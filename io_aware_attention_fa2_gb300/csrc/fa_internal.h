@@ -23,6 +23,7 @@ struct FwdParams {
   CUtensorMap tm_q;   // [B, N, H, d] viewed as 4-D (d, H, N, B); box (64, 1, 128, 1)
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  CUtensorMap tm_o;   // o as a 4-D map like tm_q (the epilogue stores O tiles through it)
   void* o;            // [B, N, H, d], same storage type as q
   float* lse;         // [B, H, N]
   int B, H, d;
