@@ -498,16 +498,24 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
       l += rs0 + rs1;
 
       if (rescale && j > x0) {
-        // P_x(j-1) V_{j-1} has completed: it was issued before S_x(j).
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t orr[32];
-          ptx::tmem_ld_32x32b_x32(tO + c * 32, orr);
-          ptx::tmem_wait_ld();
-          ptx::reg_fence(orr);
+        // P_x(j-1) V_{j-1} has completed: it was issued before S_x(j). The whole O row is
+        // loaded at once (the registers of S are free by now), so the rescale costs one TMEM
+        // round trip instead of one per 32 columns.
+        uint32_t orr[D / 32][32];
 #pragma unroll
-          for (int t = 0; t < 32; ++t) orr[t] = __float_as_uint(__uint_as_float(orr[t]) * alpha);
-          ptx::tmem_st_32x32b_x32(tO + c * 32, orr);
+        for (int c = 0; c < D / 32; ++c) ptx::tmem_ld_32x32b_x32(tO + c * 32, orr[c]);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          ptx::reg_fence(orr[c]);
+#pragma unroll
+          for (int t = 0; t < 32; t += 2) {
+            float a0 = __uint_as_float(orr[c][t]), a1 = __uint_as_float(orr[c][t + 1]);
+            ptx::mul2(a0, a1, a0, a1, alpha, alpha);
+            orr[c][t] = __float_as_uint(a0);
+            orr[c][t + 1] = __float_as_uint(a1);
+          }
+          ptx::tmem_st_32x32b_x32(tO + c * 32, orr[c]);
         }
       }
       ptx::tmem_wait_st();
