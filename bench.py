@@ -104,8 +104,12 @@ def algorithmic_bytes(w) -> int:
     return (2 * w.N + 2 * nk) * w.B * w.H * w.d * 2 + w.B * w.H * w.N * 4
 
 
-def memory_bound(w) -> bool:
-    """Decoding-style workloads (a few queries per head) are bound by reading K and V."""
+def memory_bound(w, bwd: bool = False) -> bool:
+    """Decoding-style workloads (a few queries per head) are bound by reading K and V. The
+    backward does 2.5 times the forward's FLOPs on about twice its bytes (Q, K, V, O, dO read;
+    dQ, dK, dV written), so it is compared on that ratio."""
+    if bwd:
+        return 2.5 * metric_flops(w) / (2 * algorithmic_bytes(w)) < 275.0
     return metric_flops(w) / algorithmic_bytes(w) < 275.0
 
 
@@ -637,7 +641,7 @@ def run_gpu(args, w):
                           "peak_source": "%s (burst)" % peak_src,
                           "traffic": traffic_record(w.name, "bwd" if bwd else "fwd"),
                           "algorithmic_bytes": algorithmic_bytes(w)}
-                         if not memory_bound(w) else
+                         if not memory_bound(w, bwd) else
                          {"bound": "hbm",
                           "achieved": algorithmic_bytes(w) / (kernel_ms * 1e-3) / 1e9,
                           "peak": hbm_peak, "unit": "GB/s",
@@ -662,7 +666,7 @@ def run_gpu(args, w):
             "clocks": clocks.summary(),
             "parity": parity,
         }
-        if peak_sus and not memory_bound(w):
+        if peak_sus and not memory_bound(w, bwd):
             line["roofline"]["frac_of_sustained"] = achieved / peak_sus
         if warm_ms is not None:
             line["warm_l2"] = {"ms_per_step": warm_ms, "value": flops / (warm_ms * 1e-3) / 1e12,
