@@ -53,7 +53,24 @@ __device__ int g_bwd_device_error = 0;
 
 namespace {
 
-constexpr int kBwdThreads = 320;   // producer, MMA, 4 softmax / dS' warps, 4 dQ warps
+// Warps: producer, MMA, 4 softmax / dS' warps (group 0), 4 dQ warps, and at d = 64 a second
+// group of 4 softmax / dS' warps. With two groups, the two warps of a TMEM lane quarter share
+// each key row: group g takes queries [64g, 64g + 64) of every step, which halves the length of
+// the softmax and dS' phases each thread walks. At d = 64 those phases, not the products (half
+// as long as at d = 128), set the step, and the second group gives their latencies twice the
+// warps to hide behind.
+template <int D>
+struct BwdCfg {
+  static constexpr int kSoftGroups = D == 64 ? 2 : 1;
+  static constexpr int kThreads = 320 + 128 * (kSoftGroups - 1);
+  // TMEM column of the packed P^T of 32-query chunk c (16 columns). Each group writes P over
+  // the S^T columns it has itself read (a group must not overwrite columns another group may
+  // still be loading): one group packs chunks 0..3 into columns 0..63 in order; two groups put
+  // chunks 0, 1 in columns 0..31 and chunks 2, 3 in columns 64..95.
+  static __host__ __device__ constexpr uint32_t p_col(int c) {
+    return kSoftGroups == 2 ? (c / 2) * 64 + (c % 2) * 16 : c * 16;
+  }
+};
 constexpr int kBwdStages = 2;
 constexpr uint32_t kBoxBytes = BOX_ROWS * BOX_COLS * 2;   // 16 KiB
 constexpr uint32_t kTmemCols = 512;
@@ -232,7 +249,7 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&dr)[32], const uint32_
 }
 
 template <int D, bool FP16>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
@@ -305,8 +322,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     ptx::mbar_init(bar(BB_S_FULL), 1);
     ptx::mbar_init(bar(BB_DP_FULL), 1);
-    ptx::mbar_init(bar(BB_P_FULL), 128);
-    ptx::mbar_init(bar(BB_DS_FULL), 128);
+    ptx::mbar_init(bar(BB_P_FULL), 128 * BwdCfg<D>::kSoftGroups);
+    ptx::mbar_init(bar(BB_DS_FULL), 128 * BwdCfg<D>::kSoftGroups);
     ptx::mbar_init(bar(BB_DQ_FULL), 1);
     ptx::mbar_init(bar(BB_DQ_TAKEN), 128);
     ptx::mbar_init(bar(BB_STAT), 128);
@@ -423,8 +440,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const ptx::SmemDesc do_mn = ptx::smem_desc_sw128_split(dobase(n), kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < BLOCK_M / 16; ++kk)
-          ptx::mma_f16_ts(tmem + kT_dV, tmem + kT_S + kk * 8, do_mn.at(kk * 16 * 128), id_acc,
-                          (n > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_f16_ts(tmem + kT_dV, tmem + kT_S + BwdCfg<D>::p_col(kk / 2) + (kk % 2) * 8,
+                          do_mn.at(kk * 16 * 128), id_acc, (n > 0 || kk > 0) ? 1u : 0u);
         if (!wait(BB_DS_FULL, n & 1)) { ok = false; break; }
         // S^T(i+1) over P^T(i): the softmax warps have read P^T(i) back for dS(i), and dV(i),
         // issued before, reads it first (in-order pipe).
@@ -468,9 +485,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       wait(BB_MMA_DONE, 0);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 6 || warp >= 10) {
     // ---------------------------------------------------------------- softmax / dS' warps
-    // TMEM lane r = key jb * 128 + r for S^T, dP^T, dV, dK.
+    // TMEM lane r = key jb * 128 + r for S^T, dP^T, dV, dK. Group g (warps 2..5: 0, 10..13: 1)
+    // takes the 32-query chunks [c_beg, c_end) of every step and the 32-column chunks
+    // [e_beg, e_end) of the dK, dV rows.
+    constexpr int kGroups = BwdCfg<D>::kSoftGroups;
+    const int grp_sm = warp >= 10 ? 1 : 0;
+    const int c_beg = grp_sm * (BLOCK_M / 32 / kGroups), c_end = c_beg + BLOCK_M / 32 / kGroups;
+    const int e_beg = grp_sm * (D / 32 / kGroups), e_end = e_beg + D / 32 / kGroups;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -497,17 +520,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         d_next = dpre[static_cast<int64_t>(bh) * N + q];
       }
     };
-    fetch_stats(0);
+    // Group 0 fetches and stages the statistics; every group reads them.
+    if (grp_sm == 0) fetch_stats(0);
     for (int n = 0; n < steps; ++n) {
       const int q0 = (i0 + n) * BLOCK_M;
-      // One buffer serves every step: it is refilled only after all 128 threads have
+      // One buffer serves every step: it is refilled only after every softmax thread has
       // finished the previous step's dS' (DS_FULL), the last phase that reads it.
       if (n > 0 && !wait_w(BB_DS_FULL, (n - 1) & 1)) { ok = false; break; }
-      s_lse[r] = l2_next;
-      s_d[r] = d_next;
-      ptx::mbar_arrive(bar(BB_STAT));
+      if (grp_sm == 0) {
+        s_lse[r] = l2_next;
+        s_d[r] = d_next;
+        ptx::mbar_arrive(bar(BB_STAT));
+      }
       if (!wait_w(BB_STAT, n & 1)) { ok = false; break; }
-      if (n + 1 < steps) fetch_stats(n + 1);
+      if (grp_sm == 0 && n + 1 < steps) fetch_stats(n + 1);
 
       // --- P^T: this thread's key against the 128 queries of block i, kept packed as 16-bit
       // pairs (the values the dV product uses, also used for dS'). Query q0 + t sees the key
@@ -516,9 +542,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_after_sync();
       // this step's query range of the key, relative to the block (empty when !key_ok)
       const int lo = key_ok ? q_lo - q0 : BLOCK_M, hi = key_ok ? q_hi - q0 : -1;
-      // P^T stays in TMEM (over the first 64 columns of S^T) until dS(i) has read it back.
+      // P^T stays in TMEM (over S^T columns this group has read, BwdCfg::p_col) until dS(i)
+      // has read it back.
 #pragma unroll 1
-      for (int c = 0; c < BLOCK_M / 32; ++c) {
+      for (int c = c_beg; c < c_end; ++c) {
         uint32_t sr[32];
         ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_S + c * 32, sr);
         ptx::tmem_wait_ld();
@@ -528,7 +555,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           p_chunk<true, FP16>(sr, s_lse + 32 * c, scale_log2, lo - 32 * c, hi - 32 * c, pr);
         else
           p_chunk<false, FP16>(sr, s_lse + 32 * c, scale_log2, 0, 31, pr);
-        ptx::tmem_st_32x32b_x16(tmem + lane_off + kT_S + c * 16, pr);
+        ptx::tmem_st_32x32b_x16(tmem + lane_off + kT_S + BwdCfg<D>::p_col(c), pr);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before_sync();
@@ -540,10 +567,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!wait_w(BB_DP_FULL, n & 1)) { ok = false; break; }
       ptx::tc_fence_after_sync();
 #pragma unroll 1
-      for (int c = 0; c < BLOCK_M / 32; ++c) {
+      for (int c = c_beg; c < c_end; ++c) {
         uint32_t dr[32], pw[16];
         ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + c * 32, dr);
-        ptx::tmem_ld_32x32b_x16(tmem + lane_off + kT_S + c * 16, pw);
+        ptx::tmem_ld_32x32b_x16(tmem + lane_off + kT_S + BwdCfg<D>::p_col(c), pw);
         ptx::tmem_wait_ld();
         ptx::reg_fence(dr);
         ptx::reg_fence(pw);
@@ -572,7 +599,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         ((static_cast<int64_t>(b) * N + key) * H + h) * D;
         const float f = which ? scale : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = e_beg; c < e_end; ++c) {
           uint32_t gr[32];
           ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dV + which * D + c * 32, gr);
           ptx::tmem_wait_ld();
@@ -695,7 +722,7 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_kv * bh));
-  cfg.blockDim = dim3(kBwdThreads);
+  cfg.blockDim = dim3(BwdCfg<D>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = pdl;
