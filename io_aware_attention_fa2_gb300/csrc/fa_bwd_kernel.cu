@@ -70,6 +70,16 @@ struct BwdCfg {
   static __host__ __device__ constexpr uint32_t p_col(int c) {
     return kSoftGroups == 2 ? (c / 2) * 64 + (c % 2) * 16 : c * 16;
   }
+  // d = 64 leaves TMEM columns free, so P^T gets columns of its own [kT_P, kT_P + 64) instead of
+  // sharing S^T's: then S^T(i+1) can be issued as soon as P^T(i) is written (with dV(i)), not
+  // only after dS(i) has read P^T(i) back, and the next step's P phase need not wait for it.
+  static constexpr bool kSeparateP = D == 64;
+  static constexpr uint32_t kT_P = 256 + 2 * D;
+  // TMEM column of P^T chunk c, from the allocation's base
+  static __host__ __device__ constexpr uint32_t p_at(int c) {
+    return kSeparateP ? kT_P + c * 16 : p_col(c);   // (kT_S = 0)
+  }
+  static_assert(!kSeparateP || kT_P + 64 <= 512, "TMEM columns");
 };
 constexpr int kBwdStages = 2;
 constexpr uint32_t kBoxBytes = BOX_ROWS * BOX_COLS * 2;   // 16 KiB
@@ -440,17 +450,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const ptx::SmemDesc do_mn = ptx::smem_desc_sw128_split(dobase(n), kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < BLOCK_M / 16; ++kk)
-          ptx::mma_f16_ts(tmem + kT_dV, tmem + kT_S + BwdCfg<D>::p_col(kk / 2) + (kk % 2) * 8,
+          ptx::mma_f16_ts(tmem + kT_dV, tmem + BwdCfg<D>::p_at(kk / 2) + (kk % 2) * 8,
                           do_mn.at(kk * 16 * 128), id_acc, (n > 0 || kk > 0) ? 1u : 0u);
-        if (!wait(BB_DS_FULL, n & 1)) { ok = false; break; }
-        // S^T(i+1) over P^T(i): the softmax warps have read P^T(i) back for dS(i), and dV(i),
-        // issued before, reads it first (in-order pipe).
-        if (next) {
-          if (!wait(BB_QD_FULL + (n + 1) % kBwdStages, ((n + 1) / kBwdStages) & 1)) {
-            ok = false;
-            break;
+        if constexpr (BwdCfg<D>::kSeparateP) {
+          // S^T(i+1) right away: the softmax warps have read S^T(i) (P^T(i) is written), and
+          // P^T(i) lives in columns of its own. P^T(i+1) is written only after S^T(i+1) has
+          // completed, and so has dV(i), issued before it (in-order pipe).
+          if (next) {
+            if (!wait(BB_QD_FULL + (n + 1) % kBwdStages, ((n + 1) / kBwdStages) & 1)) {
+              ok = false;
+              break;
+            }
+            issue_s(n + 1);
           }
-          issue_s(n + 1);
+        }
+        if (!wait(BB_DS_FULL, n & 1)) { ok = false; break; }
+        if constexpr (!BwdCfg<D>::kSeparateP) {
+          // S^T(i+1) over P^T(i): the softmax warps have read P^T(i) back for dS(i), and
+          // dV(i), issued before, reads it first (in-order pipe).
+          if (next) {
+            if (!wait(BB_QD_FULL + (n + 1) % kBwdStages, ((n + 1) / kBwdStages) & 1)) {
+              ok = false;
+              break;
+            }
+            issue_s(n + 1);
+          }
         }
         ptx::tc_fence_after_sync();
         // dQ first, into T_dP (dP^T(i) is in the softmax threads' registers by now), so that
@@ -555,7 +579,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           p_chunk<true, FP16>(sr, s_lse + 32 * c, scale_log2, lo - 32 * c, hi - 32 * c, pr);
         else
           p_chunk<false, FP16>(sr, s_lse + 32 * c, scale_log2, 0, 31, pr);
-        ptx::tmem_st_32x32b_x16(tmem + lane_off + kT_S + BwdCfg<D>::p_col(c), pr);
+        ptx::tmem_st_32x32b_x16(tmem + lane_off + BwdCfg<D>::p_at(c), pr);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before_sync();
@@ -570,7 +594,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       for (int c = c_beg; c < c_end; ++c) {
         uint32_t dr[32], pw[16];
         ptx::tmem_ld_32x32b_x32(tmem + lane_off + kT_dP + c * 32, dr);
-        ptx::tmem_ld_32x32b_x16(tmem + lane_off + kT_S + BwdCfg<D>::p_col(c), pw);
+        ptx::tmem_ld_32x32b_x16(tmem + lane_off + BwdCfg<D>::p_at(c), pw);
         ptx::tmem_wait_ld();
         ptx::reg_fence(dr);
         ptx::reg_fence(pw);
