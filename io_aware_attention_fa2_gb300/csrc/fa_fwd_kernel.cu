@@ -65,15 +65,20 @@ constexpr float kRescaleLog2 = 8.0f;
 
 // Shape of one CTA. QT = 2: two Q tiles (A, B) whose softmax phases alternate on the tensor
 // pipe; 512 TMEM columns (S_A, S_B, O_A, O_B), one CTA per SM. QT = 1 (d = 64 only): one Q
-// tile, S 128 + O 64 columns in a 256-column allocation, 6 warps and 80 KiB of shared memory,
-// so that two CTAs share an SM and one's start and end overlap the other's main loop.
+// tile, S 128 + O 64 + P 64 columns in a 256-column allocation, 6 warps and 80 KiB of shared
+// memory, so that two CTAs share an SM; with P in columns of its own, S(j+1) is computed while
+// the softmax of S(j) runs and P(j) V_j while the softmax of S(j+1) runs.
 template <int QT, int D>
 struct Cfg {
   static constexpr int kThreads = 64 + 128 * QT;
-  static constexpr int kMinBlocks = QT == 2 ? 1 : 2;
+  static constexpr int kMinBlocks = QT == 1 && D == 64 ? 2 : 1;
   static constexpr uint32_t kTmemO = 128 * QT;                     // O_X at kTmemO + x * D
-  static constexpr uint32_t kTmemCols = QT == 2 ? 512 : 256;
-  static_assert(kTmemO + QT * D <= kTmemCols, "TMEM columns");
+  static constexpr uint32_t kTmemCols = QT == 1 && D == 64 ? 256 : 512;
+  // QT = 1: P in columns of its own after O (S 128 + O 64 + P 64 = 256), so that S(j+1) can
+  // be computed while the softmax of S(j) runs. QT = 2: P is written over S.
+  static constexpr bool kSeparateP = QT == 1;
+  static constexpr uint32_t kTmemP = kTmemO + QT * D;
+  static_assert(kTmemO + QT * D + (kSeparateP ? 64 : 0) <= kTmemCols, "TMEM columns");
 };
 
 template <int QT, int D>
@@ -100,7 +105,8 @@ enum : int {
   BAR_O_DONE = BAR_P_FULL + kMaxQTiles,   // + tile: P_X(j) V_j computed
   BAR_MMA_DONE = BAR_O_DONE + kMaxQTiles,
   BAR_O_STAGED = BAR_MMA_DONE + 1,        // + tile: the tile's O rows are in shared memory
-  BAR_COUNT = BAR_O_STAGED + kMaxQTiles
+  BAR_S_READ = BAR_O_STAGED + kMaxQTiles, // one-tile CTA: S(j) loaded by the softmax (128)
+  BAR_COUNT = BAR_S_READ + 1
 };
 static_assert(BAR_COUNT <= 24, "barrier slots");
 
@@ -250,6 +256,7 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
       ptx::mbar_init(bar(BAR_O_DONE + x), 1);
       ptx::mbar_init(bar(BAR_O_STAGED + x), 128);
     }
+    ptx::mbar_init(bar(BAR_S_READ), 128);
     ptx::mbar_init(bar(BAR_MMA_DONE), 1);
     ptx::fence_barrier_init();
   }
@@ -343,7 +350,8 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
             ptx::smem_desc_sw128_split(sV + ((j - u0) % kStages) * L::kTile, kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-          ptx::mma_f16_ts(tmem + kTmemO + x * D, tmem + x * BLOCK_N + kk * 8,
+          ptx::mma_f16_ts(tmem + kTmemO + x * D,
+                          tmem + (C::kSeparateP ? C::kTmemP : x * BLOCK_N) + kk * 8,
                           v_desc.at(kk * 16 * 128), idesc_pv, (!first || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar(BAR_O_DONE + x));
       };
@@ -366,9 +374,25 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
           ptx::mma_commit(bar(BAR_K_EMPTY + 0));
         }
       }
+      if constexpr (C::kSeparateP) {
+        // One tile, P in columns of its own: S(j+1) is issued once the softmax has loaded S(j)
+        // (S_READ), so it is computed while that softmax runs; P(j) V_j once P(j) is stored.
+        // The softmax waits for P(j-1) V_{j-1} (O_DONE) before it writes P(j) or rescales O.
+        for (int j = u0; ok && any_work && j < u1; ++j) {
+          const int s = (j - u0) % kStages;
+          if (j + 1 < u1) {
+            if (!wait_k(j + 1) || !wait(BAR_S_READ, (j - a0) & 1)) { ok = false; break; }
+            issue_s(0, j + 1);
+            ptx::mma_commit(bar(BAR_K_EMPTY + (j + 1 - u0) % kStages));
+          }
+          if (!wait_v(j) || !wait(BAR_P_FULL + 0, (j - a0) & 1)) { ok = false; break; }
+          issue_pv(0, j, j == a0);
+          ptx::mma_commit(bar(BAR_V_EMPTY + s));
+        }
+      }
       // Per K/V tile j: P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1). The softmax of one tile
       // runs while the tensor pipe works on the other.
-      for (int j = u0; ok && any_work && j < u1; ++j) {
+      for (int j = u0; !C::kSeparateP && ok && any_work && j < u1; ++j) {
         const int s = (j - u0) % kStages;
         const bool next = j + 1 < u1;
         if (!wait_v(j)) { ok = false; break; }
@@ -402,6 +426,8 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
     const int x0 = x ? b0 : a0, x1 = x ? b1 : a1;       // this tile's K/V tiles [x0, x1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + x * BLOCK_N;
+    // where P_x(j) goes: columns of its own (one-tile CTA) or over S_x
+    const uint32_t tP = C::kSeparateP ? tmem + lane_off + C::kTmemP : tS;
     const uint32_t tO = tmem + lane_off + kTmemO + x * D;
     const bool scale_pos = scale_log2 > 0.f;
     // This row's allowed keys [row_lo, row_hi); a K/V tile starting at k0 needs no per-element
@@ -422,6 +448,11 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
 #pragma unroll
       for (int c = 0; c < BLOCK_N / 32; ++c) ptx::tmem_ld_32x32b_x32(tS + c * 32, sr[c]);
       ptx::tmem_wait_ld();
+      if constexpr (C::kSeparateP) {
+        // S_x(j) is in registers: the MMA thread may compute S_x(j+1) over it
+        ptx::tc_fence_before_sync();
+        ptx::mbar_arrive(bar(BAR_S_READ));
+      }
       float s[BLOCK_N];
 #pragma unroll
       for (int c = 0; c < BLOCK_N / 32; ++c) {
@@ -470,10 +501,22 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
         m = m_new;
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
+      if constexpr (C::kSeparateP) {
+        // P_x(j-1) V_{j-1} reads the P columns and accumulates into O: both must be done
+        // before P_x(j) is written or O rescaled (S_x(j) no longer implies it here).
+        if (j > x0) {
+          if (!ptx::wait_bounded_warp(bar(BAR_O_DONE + x), (j - 1 - x0) & 1, abort_p,
+                                      kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+        }
+      }
 
-      // P_x(j) = 2^(scaled score - m) -> TMEM over the first 64 columns of S_x, 32 keys (16
-      // columns) at a time: column c holds keys 2c (low half) and 2c + 1 (high half), rounded
-      // to the input type.
+      // P_x(j) = 2^(scaled score - m) -> TMEM (over the first 64 columns of S_x, or the P
+      // columns of the one-tile CTA), 32 keys (16 columns) at a time: column c holds keys 2c
+      // (low half) and 2c + 1 (high half), rounded to the input type.
       // exponent argument: s * scale_log2 - m_use (positive scale, folded into one FMA) or
       // s - m_use (s already scaled)
       float rs0 = 0.f, rs1 = 0.f;
@@ -493,14 +536,14 @@ __global__ void __launch_bounds__((Cfg<QT, D>::kThreads), (Cfg<QT, D>::kMinBlock
           ptx::add2(rs0, rs1, rs0, rs1, p0, p1);
           pr[t] = pack2<FP16>(p0, p1);
         }
-        ptx::tmem_st_32x32b_x16(tS + c * 16, pr);
+        ptx::tmem_st_32x32b_x16(tP + c * 16, pr);
       }
       l += rs0 + rs1;
 
       if (rescale && j > x0) {
-        // P_x(j-1) V_{j-1} has completed: it was issued before S_x(j). The whole O row is
-        // loaded at once (the registers of S are free by now), so the rescale costs one TMEM
-        // round trip instead of one per 32 columns.
+        // P_x(j-1) V_{j-1} has completed: it was issued before S_x(j) (one-tile CTA: waited
+        // for above). The whole O row is loaded at once (the registers of S are free by
+        // now), so the rescale costs one TMEM round trip instead of one per 32 columns.
         uint32_t orr[D / 32][32];
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) ptx::tmem_ld_32x32b_x32(tO + c * 32, orr[c]);
@@ -700,15 +743,13 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-// Sequences up to this many queries use one Q tile per CTA at d = 64 (two CTAs per SM).
-// Measured at B=4, H=16, N=1024: causal 32.7 -> 30.2 us, non-causal unchanged; at N = 2048
-// and longer the two-tile CTA is as fast or faster.
-constexpr int kOneTileMaxNq = 1024;
-
 template <bool WINDOWED>
 cudaError_t launch_dtype(const FwdParams& p, cudaStream_t stream) {
   if (p.d == 64) {
-    if (p.num_splits == 1 && p.Nq <= kOneTileMaxNq)
+    // d = 64 (not split): one Q tile per CTA, P in columns of its own, two CTAs per SM. Against
+    // the two-tile CTA: B=4 H=16 N=1K 39 -> 34 us; B=2 H=16 N=8K causal 359 -> 291 us,
+    // non-causal 671 -> 557 us.
+    if (p.num_splits == 1)
       return p.fp16 ? launch_impl<1, 64, true, WINDOWED>(p, stream)
                     : launch_impl<1, 64, false, WINDOWED>(p, stream);
     return p.fp16 ? launch_impl<2, 64, true, WINDOWED>(p, stream)
