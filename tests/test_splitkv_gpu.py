@@ -53,6 +53,14 @@ def test_decode(Nk, splits, causal):
     case(2, 4, 1, Nk, 128, "bf16", causal, splits, seed=600 + Nk)
 
 
+@pytest.mark.parametrize("Nk", [1, 1000])
+@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_d64(Nk, splits, causal):
+    """One query at d = 64: unsplit it takes the one-Q-tile kernel, split the two-tile one."""
+    case(2, 4, 1, Nk, 64, "bf16", causal, splits, seed=650 + Nk)
+
+
 @pytest.mark.parametrize("Nq,Nk", [(16, 2000), (129, 700), (300, 300), (513, 1100)])
 @pytest.mark.parametrize("splits", [1, 4])
 @pytest.mark.parametrize("causal", [False, True])
