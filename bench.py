@@ -249,6 +249,7 @@ class OracleSampler:
         self.total_rows = w.B * w.H * w.N
         self.rng = np.random.Generator(np.random.PCG64(w.seed + 11))
         self.rows_per_s = None
+        self.fixed_s = 0.0
 
     def pick(self, n):
         w = self.w
@@ -267,11 +268,19 @@ class OracleSampler:
         return metric_flops(w) * (len(rows) / self.total_rows), dt, len(rows)
 
     def rows_for(self, seconds, min_rows=16):
+        """Rows that take about `seconds` in one call. Every call first decodes the inputs (a
+        cost independent of the rows), so the rate is taken from two calls of different sizes
+        and that cost is set apart."""
         if self.rows_per_s is None:
-            n = 64
-            _, dt, n = self.run(n)
-            self.rows_per_s = n / max(dt, 1e-4)
-        return int(min(self.total_rows, max(min_rows, self.rows_per_s * seconds)))
+            _, dt1, n1 = self.run(64)
+            _, dt2, n2 = self.run(512)
+            per_row = (dt2 - dt1) / max(n2 - n1, 1)
+            if per_row <= 0:
+                per_row = dt2 / max(n2, 1)
+            self.fixed_s = max(dt1 - n1 * per_row, 0.0)
+            self.rows_per_s = 1.0 / max(per_row, 1e-9)
+        budget = max(seconds - self.fixed_s, 0.0)
+        return int(min(self.total_rows, max(min_rows, self.rows_per_s * budget)))
 
     def cores(self):
         return self.oracle.max_threads(self.lib)
