@@ -40,6 +40,11 @@
 // offset, so O / l and m + log2(l) are exact in real arithmetic.
 //
 // TMEM columns (512 allocated): S_A [0,128), S_B [128,256), O_A [256,256+d), O_B [256+d,256+2d).
+//
+// The one-tile CTA (d = 64 without split K/V; Cfg below) runs tile A alone with warps 2..5 and
+// two CTAs per SM: TMEM (256 allocated) S [0,128), O [128,192), P [192,256). With P in columns
+// of its own, S(j+1) is issued as soon as the softmax has loaded S(j), and the softmax waits for
+// P(j-1) V_{j-1} before it writes P(j) or rescales O.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
