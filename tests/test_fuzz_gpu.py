@@ -111,3 +111,57 @@ def test_fuzz_backward(i):
                              window=c["window"], seqlens_k=c["lens"])
     for j, (name, g, r) in enumerate(zip(("dq", "dk", "dv"), grads, refs)):
         check_grad(name, g.double().cpu().numpy(), r, dtype, c, allow if j == 0 else None)
+
+
+N_HOST = 16
+
+
+def host_tensor(bits: np.ndarray, dtype: str):
+    """A CPU tensor (pinned) of the bit patterns."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.bfloat16 if dtype == "bf16" else torch.float16).pin_memory()
+
+
+@pytest.mark.parametrize("i", range(N_HOST))
+def test_fuzz_host_forward(i):
+    """The host-buffer forward (copies in and out around the kernels, head groups overlapped)."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import attention_forward
+    c = draw(100 + i, bwd=True)   # queries and keys share N on the host-buffer path
+    qb, kb, vb = make_qkv(c["B"], c["H"], c["nq"], c["d"], c["dtype"], c["seed"])
+    lens_t = None if c["lens"] is None else torch.tensor(c["lens"], dtype=torch.int32)
+    o, lse = attention_forward(*(host_tensor(x, c["dtype"]) for x in (qb, kb, vb)),
+                               causal=c["causal"], scale=c["scale"], window=c["window"],
+                               seqlens_k=lens_t)
+    assert not o.is_cuda and not lse.is_cuda
+    o_ref, lse_ref = oracle.attention(qb, kb, vb, c["causal"], c["scale"], dtype=c["dtype"],
+                                      window=c["window"], seqlens_k=c["lens"])
+    a_ref, _ = attention_aux(qb, kb, vb, c["causal"], c["scale"], c["dtype"], None, c["window"],
+                             c["lens"])
+    check(o.double().numpy(), lse.double().numpy(), o_ref, lse_ref, c, c["dtype"], a_ref)
+
+
+@pytest.mark.parametrize("i", range(N_HOST // 2))
+def test_fuzz_host_backward(i):
+    """The host-buffer backward on the host-buffer forward's O and LSE."""
+    import torch
+
+    from io_aware_attention_fa2_gb300 import attention_backward, attention_forward
+    c = draw(200 + i, bwd=True)
+    B, H, N, d, dtype = c["B"], c["H"], c["nq"], c["d"], c["dtype"]
+    qb, kb, vb = make_qkv(B, H, N, d, dtype, c["seed"])
+    dob = round_to_bits(normal((B, N, H, d), c["seed"] + 1), dtype)
+    q, k, v, do = (host_tensor(x, dtype) for x in (qb, kb, vb, dob))
+    lens_t = None if c["lens"] is None else torch.tensor(c["lens"], dtype=torch.int32)
+    kw = dict(causal=c["causal"], scale=c["scale"], window=c["window"], seqlens_k=lens_t)
+    o, lse = attention_forward(q, k, v, **kw)
+    grads = attention_backward(q, k, v, o, do, lse, **kw)
+    refs = oracle.attention_bwd(qb, kb, vb, dob, c["causal"], c["scale"], dtype=dtype,
+                                window=c["window"], seqlens_k=c["lens"])
+    allow = dq_allowance_for(qb, kb, vb, dob, c["causal"], c["scale"], dtype,
+                             window=c["window"], seqlens_k=c["lens"])
+    for j, (name, g, r) in enumerate(zip(("dq", "dk", "dv"), grads, refs)):
+        assert not g.is_cuda
+        check_grad(name, g.double().numpy(), r, dtype, c, allow if j == 0 else None)
