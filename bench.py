@@ -559,14 +559,14 @@ def run_gpu(args, w):
                 print(json.dumps({"error": "parity failed", "parity": parity}), flush=True)
                 return 3
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(dev)
-
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clocks:
+        # The warm-up steps run right before the timed ones, after the sampler has started: a
+        # step that follows an idle GPU (the sampler's start-up) ran 2-20 % slower than the rest.
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
